@@ -1,0 +1,346 @@
+"""Benchmark of the speculative-decoding verify step on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one synthetic batch: verify
+attention for every layer, argmax + greedy accept, and the KV commit of all
+layers.  The default workload is the 8-draft chain verify at 4096 tokens of
+context (16 layers, 24/4 heads, d = 256, bf16 paged KV with a permuted page
+table, logits [9, 151936]); ``--config`` picks another one.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
+baseline arm), on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verify_decode_gb300 import native, synth  # noqa: E402
+from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inputs  # noqa: E402
+
+METRIC = "verify steps/s"
+DEFAULT_CONFIG = "chain8_ctx4k"
+ATTN_SRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", "attn_mma.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def attn_bytes_per_layer(w) -> int:
+    """Algorithmic bytes of one layer's verify attention.
+
+    Context K and V are read once (2 x 4 heads x 256 x 2 B = 4096 B per token),
+    plus Q, the draft K/V, the output and the page-table entries.
+    """
+    ctx = int(np.asarray(w.ctx_lens, dtype=np.int64).sum())
+    pages = int(sum((int(L) + 15) // 16 for L in w.ctx_lens))
+    n = w.total_nodes
+    return ctx * 4096 + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
+
+
+def kernel_sha() -> str:
+    with open(ATTN_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def traffic_for(config: str):
+    """dram bytes per attention launch from the last ncu capture, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == config:
+                    return float(parts[2]) if parts[1] == kernel_sha() else None
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    native.load()
+    w = synth.make_workload(args.config, device=dev)
+    d = device_inputs(w, dev)
+    step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev)
+    run_args = (w.q, w.k_cache, w.v_cache, w.k_new, w.v_new, d["page_table"], d["ctx_lens"], d["parents"],
+                d["draft_tokens"], w.logits)
+    step.run(*run_args)                       # eager once: surfaces launch errors early
+    torch.cuda.synchronize(dev)
+    graph = step.capture(*run_args)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    status = int(step.dev_status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    accepted = int(step.accept_len.sum().item())
+
+    # ---- timed region: K steps, graph replays back to back
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms, world, dev)
+    ms_per_step = ms / args.steps
+
+    # ---- the dominant kernel (one layer's verify attention), events around each launch
+    reps = max(20, args.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        layer = i % w.layers
+        evs[i][0].record(stream)
+        step.attention(layer, w.q[layer], w.k_cache[layer], w.v_cache[layer], w.k_new[layer], w.v_new[layer],
+                       d["page_table"], d["ctx_lens"], d["parents"])
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peak, peak_kind = peaks()
+    alg = attn_bytes_per_layer(w)
+    achieved = alg / (attn_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API: host inputs in, host results out
+    pin = lambda t: t.detach().to("cpu").pin_memory()
+    host_in = ([pin(x) for x in w.q] + [pin(x) for x in w.k_new] + [pin(x) for x in w.v_new] +
+               [pin(w.logits), pin(d["parents"]), pin(d["draft_tokens"])])
+    dev_in = list(w.q) + list(w.k_new) + list(w.v_new) + [w.logits, d["parents"], d["draft_tokens"]]
+    outs = [step.accept_len, step.path, step.out_tokens, step.new_ctx_lens]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    e2e_steps = max(5, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        graph.replay()
+        for dsrc, hdst in zip(outs, host_out):
+            hdst.copy_(dsrc, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+
+    line = {
+        "metric": METRIC,
+        "value": world * 1000.0 / ms_per_step,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; Q/K/V ~ N(0,1)/16 bf16, planted-argmax fp32 logits)",
+        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers,
+                   "ctx_lens": [int(x) for x in w.ctx_lens][:8], "draft_nodes": w.total_nodes,
+                   "vocab": w.vocab, "heads": "24q/4kv", "head_dim": 256, "page": 16,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (KV read per step exceeds 129 MB)",
+                   "cuda_graph": True},
+        "accepted_tokens_per_step": accepted,
+        "accepted_tok_per_s": world * accepted * 1000.0 / ms_per_step,
+        "kv_read_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_for(args.config),
+                     "kernel": "verify attention (split + merge), one layer",
+                     "alg_bytes_per_launch": alg, "launch_ms": attn_ms, "peak_kind": peak_kind},
+        "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.config, reps=1)
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+def cpu_baseline(w, config: str, reps: int = 1) -> dict:
+    """Time the oracle on a bounded sample: one layer's attention + accept + commit.
+
+    A step is extrapolated as layers x attention + accept + commit.
+    """
+    import oracle
+    f32 = lambda t: t.detach().to("cpu", torch.float32).numpy()
+    layer = 0
+    host = dict(q=f32(w.q[layer]), kc=f32(w.k_cache[layer]), vc=f32(w.v_cache[layer]),
+                kn=f32(w.k_new[layer]), vn=f32(w.v_new[layer]))
+    logits = w.logits.detach().cpu().numpy()
+    t_attn, t_acc, t_com = [], [], []
+    for _ in range(reps):
+        t = time.perf_counter()
+        oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
+                                w.ctx_lens, w.q_indptr, w.parents)
+        t_attn.append(time.perf_counter() - t)
+        t = time.perf_counter()
+        _, lens, paths, _ = oracle.accept(w.q_indptr, w.parents, w.draft_tokens, logits)
+        t_acc.append(time.perf_counter() - t)
+        t = time.perf_counter()
+        oracle.kv_commit([host["kc"]], [host["vc"]], [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens,
+                         w.q_indptr, lens, paths)
+        t_com.append(time.perf_counter() - t)
+    step_s = w.layers * statistics.mean(t_attn) + statistics.mean(t_acc) + w.layers * statistics.mean(t_com)
+    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{config}: {reps} x (1 layer attention + accept + 1 layer commit) on the host, "
+                      f"extrapolated to {w.layers} layers; numpy fp64",
+            "attn_s_per_layer": statistics.mean(t_attn), "accept_s": statistics.mean(t_acc)}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return None
+    dev = "cpu"
+    w = synth.make_workload(args.config, device=dev)
+    reps = max(1, args.steps)
+    base = cpu_baseline(w, args.config, reps=1)          # warm-up sample
+    t = time.perf_counter()
+    base = cpu_baseline(w, args.config, reps=reps)
+    wall = time.perf_counter() - t
+    v = base["value"]
+    return {"metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "vocab": w.vocab},
+            "impl": "reference", "cpu_baseline": {**base, "wall_s": wall},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

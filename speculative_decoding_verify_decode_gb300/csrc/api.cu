@@ -1,0 +1,218 @@
+// C-ABI entry points (declared in include/sd_verify.h): host-side argument
+// checks, workspace layout, split-KV sizing, and the kernel launches.  Nothing
+// here allocates device memory or synchronises; every launch goes on the
+// caller's stream.
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace sdv;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+sd_status fill_batch(int batch, const int* indptr, BatchDesc* bd) {
+  if (batch < 1 || batch > kMaxBatch || indptr == nullptr) return SD_ERR_INVALID_ARG;
+  if (indptr[0] != 0) return SD_ERR_INVALID_ARG;
+  bd->batch = batch;
+  bd->max_nodes = 0;
+  for (int b = 0; b <= batch; ++b) bd->q_indptr[b] = indptr[b];
+  for (int b = 0; b < batch; ++b) {
+    const int n = indptr[b + 1] - indptr[b];
+    if (n < 1) return SD_ERR_INVALID_ARG;
+    if (n > kMaxNodes) return SD_ERR_UNSUPPORTED;
+    if (n > bd->max_nodes) bd->max_nodes = n;
+  }
+  bd->total_nodes = indptr[batch];
+  return SD_OK;
+}
+
+sd_status check_shape(const sd_shape* s, BatchDesc* bd) {
+  if (s == nullptr) return SD_ERR_INVALID_ARG;
+  if (s->num_q_heads != kHq || s->num_kv_heads != kHkv || s->head_dim != kDim || s->page_size != kPage)
+    return SD_ERR_UNSUPPORTED;
+  if (s->max_pages_per_seq < 1 || s->num_pool_pages < 1 || s->num_splits < 0) return SD_ERR_INVALID_ARG;
+  if ((long long)s->max_pages_per_seq * kPage > (1LL << 30)) return SD_ERR_UNSUPPORTED;
+  return fill_batch(s->batch, s->q_indptr_h, bd);
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();  // no device here: size for a 152-SM part
+    return 152;
+  }
+  return sms;
+}
+
+struct SplitPlan {
+  int chunk;     // context tokens per split
+  int nsplit;    // splits in the grid
+};
+
+// Context tokens per split: enough CTAs for about two per SM, but at least
+// four context tokens per query row so that the partial outputs (1 KB per
+// row) stay well below the K/V bytes the split reads (1 KB per token).
+SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
+  const int tile = attn_mma_tile();
+  const long long max_ctx = (long long)s->max_pages_per_seq * kPage;
+  long long want = s->num_splits;
+  if (want == 0) {
+    const int ctas = attn_mma_ctas_per_split(bd);
+    want = (2LL * device_sm_count() + ctas - 1) / ctas;
+  }
+  long long chunk = (max_ctx + want - 1) / want;
+  if (s->num_splits == 0) {
+    const long long min_chunk = 4LL * bd.max_nodes * kGroup;
+    if (chunk < min_chunk) chunk = min_chunk;
+  }
+  chunk = (chunk + tile - 1) / tile * tile;
+  if (chunk < tile) chunk = tile;
+  long long n = (max_ctx + chunk - 1) / chunk;
+  if (n < 1) n = 1;
+  return SplitPlan{(int)chunk, (int)n};
+}
+
+size_t attn_workspace(const SplitPlan& pl, const BatchDesc& bd) {
+  if (pl.nsplit <= 1) return 0;
+  const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
+  return align_up(rows * kDim * sizeof(float)) + align_up(rows * sizeof(float));
+}
+
+sd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SD_OK : SD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sd_status_string(sd_status s) {
+  switch (s) {
+    case SD_OK: return "ok";
+    case SD_ERR_INVALID_ARG: return "invalid argument";
+    case SD_ERR_UNSUPPORTED: return "unsupported shape";
+    case SD_ERR_CUDA: return "CUDA error";
+    case SD_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t sd_verify_attn_workspace_size(const sd_shape* shape) {
+  BatchDesc bd;
+  if (check_shape(shape, &bd) != SD_OK) return 0;
+  return attn_workspace(plan_splits(shape, bd), bd);
+}
+
+sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                         const void* k_new, const void* v_new, const int* page_table, const int* ctx_lens,
+                         const int* parents, void* out, float* lse, void* workspace, size_t ws_bytes,
+                         int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = check_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (!q || !k_cache || !v_cache || !k_new || !v_new || !page_table || !ctx_lens || !parents || !out)
+    return SD_ERR_INVALID_ARG;
+  const SplitPlan pl = plan_splits(shape, bd);
+  const size_t need = attn_workspace(pl, bd);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SD_ERR_WORKSPACE;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.page_table = page_table;
+  p.ctx_lens = ctx_lens;
+  p.parents = parents;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.dev_status = dev_status;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pool_pages = shape->num_pool_pages;
+  p.chunk = pl.chunk;
+  p.num_splits = pl.nsplit;
+  if (need > 0) {
+    const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(float)));
+  }
+  return cuda_status(launch_attn_mma(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sd_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {
+  BatchDesc bd;
+  if (fill_batch(batch, q_indptr_h, &bd) != SD_OK || vocab < 1) return 0;
+  const size_t chunks = ((size_t)vocab + kAcceptChunk - 1) / kAcceptChunk;
+  return align_up((size_t)bd.total_nodes * chunks * 8);
+}
+
+sd_status sd_accept(int batch, const int* q_indptr_h, int vocab, const float* logits, const int* parents,
+                    const int* draft_tokens, int* accept_len, int* path, int* out_tokens, int* target_tokens,
+                    int max_path, void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = fill_batch(batch, q_indptr_h, &bd);
+  if (st != SD_OK) return st;
+  if (vocab < 1 || max_path < 1 || !logits || !parents || !draft_tokens || !accept_len || !path || !out_tokens)
+    return SD_ERR_INVALID_ARG;
+  const size_t need = sd_accept_workspace_size(batch, q_indptr_h, vocab);
+  if (workspace == nullptr || ws_bytes < need) return SD_ERR_WORKSPACE;
+  AcceptParams p;
+  p.logits = logits;
+  p.parents = parents;
+  p.draft_tokens = draft_tokens;
+  p.accept_len = accept_len;
+  p.path = path;
+  p.out_tokens = out_tokens;
+  p.target_tokens = target_tokens;
+  p.dev_status = dev_status;
+  p.partial = workspace;
+  p.vocab = vocab;
+  p.chunks = (vocab + kAcceptChunk - 1) / kAcceptChunk;
+  p.max_path = max_path;
+  return cuda_status(launch_accept(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
+sd_status sd_kv_commit(const sd_shape* shape, int num_layers, void* const* k_cache_layers,
+                       void* const* v_cache_layers, const void* const* k_new_layers,
+                       const void* const* v_new_layers, const int* page_table, const int* ctx_lens,
+                       int* new_ctx_lens, const int* accept_len, const int* path, int max_path,
+                       int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = check_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (num_layers < 1) return SD_ERR_INVALID_ARG;
+  if (num_layers > kMaxLayers) return SD_ERR_UNSUPPORTED;
+  if (!k_cache_layers || !v_cache_layers || !k_new_layers || !v_new_layers || !page_table || !ctx_lens ||
+      !accept_len || !path || max_path < 1)
+    return SD_ERR_INVALID_ARG;
+  if (new_ctx_lens != nullptr && new_ctx_lens == ctx_lens) return SD_ERR_INVALID_ARG;
+  CommitParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_cache_layers[l] || !v_cache_layers[l] || !k_new_layers[l] || !v_new_layers[l])
+      return SD_ERR_INVALID_ARG;
+    p.k_cache[l] = k_cache_layers[l];
+    p.v_cache[l] = v_cache_layers[l];
+    p.k_new[l] = k_new_layers[l];
+    p.v_new[l] = v_new_layers[l];
+  }
+  p.page_table = page_table;
+  p.ctx_lens = ctx_lens;
+  p.new_ctx_lens = new_ctx_lens;
+  p.accept_len = accept_len;
+  p.path = path;
+  p.dev_status = dev_status;
+  p.max_path = max_path;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pool_pages = shape->num_pool_pages;
+  p.num_layers = num_layers;
+  return cuda_status(launch_commit(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Shared constants, parameter blocks and small device helpers of the verify
+// kernels.  Internal to the library (the public interface is sd_verify.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/sd_verify.h"
+
+namespace sdv {
+
+constexpr int kHq = 24;          // query heads
+constexpr int kHkv = 4;          // KV heads
+constexpr int kGroup = kHq / kHkv;
+constexpr int kDim = 256;        // head_dim
+constexpr int kPage = 16;        // tokens per KV page
+constexpr int kMaxNodes = SD_MAX_NODES;
+constexpr int kMaxBatch = SD_MAX_BATCH;
+constexpr int kMaxLayers = SD_MAX_LAYERS;
+
+// log2(e) / sqrt(256): scores are kept in base 2 so exp becomes ex2.
+constexpr float kScaleLog2 = 1.4426950408889634f / 16.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Per-call batch description passed by value to every kernel.
+struct BatchDesc {
+  int batch;
+  int total_nodes;
+  int max_nodes;
+  int q_indptr[kMaxBatch + 1];
+};
+
+// Attention launch parameters (one layer).
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int* page_table;
+  const int* ctx_lens;
+  const int* parents;
+  __nv_bfloat16* out;
+  float* lse;            // nullable
+  float* o_part;         // [num_splits][total_nodes][24][256]
+  float* lse_part;       // [num_splits][total_nodes][24]  (base-2 log-sum-exp)
+  int* dev_status;       // nullable
+  int max_pages;
+  int num_pool_pages;
+  int chunk;             // context tokens per split (multiple of the kernel's tile)
+  int num_splits;
+};
+
+__device__ __forceinline__ void report(int* status, int bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Number of active splits of a sequence with context length L (>= 1: the
+// first split also carries the draft block, even when L == 0).
+__host__ __device__ __forceinline__ int active_splits(int L, int chunk) {
+  int n = (L + chunk - 1) / chunk;
+  return n < 1 ? 1 : n;
+}
+
+}  // namespace sdv

@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+the header declares, and rejects bad host-side arguments before any launch.
+
+Every call below fails a host check, so no kernel is ever launched with the
+placeholder pointers used here.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from speculative_decoding_verify_decode_gb300 import build, native
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sd_verify.h")
+FAKE = 0x10000   # never dereferenced: each call returns before launching
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return native.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = set(re.findall(r"\b(sd_[a-z_]+)\s*\(", open(HEADER).read()))
+    assert {"sd_verify_attn", "sd_accept", "sd_kv_commit", "sd_status_string"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert native.status_string(0) == "ok"
+    assert "workspace" in native.status_string(4)
+
+
+def _shape(indptr=(0, 5), **kw):
+    s = native.Shape(list(indptr), kw.pop("max_pages", 40), kw.pop("pool", 40), kw.pop("splits", 0))
+    for k, v in kw.items():
+        setattr(s.c, k, v)
+    return s
+
+
+def _attn(lib, shape, ws=None, ws_bytes=0, q=FAKE):
+    return lib.sd_verify_attn(shape.ref, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, ws, ws_bytes,
+                              None, None)
+
+
+def test_geometry_other_than_24_4_256_16_is_unsupported(lib):
+    for field, bad in [("num_q_heads", 32), ("num_kv_heads", 8), ("head_dim", 128), ("page_size", 64)]:
+        assert _attn(lib, _shape(**{field: bad})) == native.SD_ERR_UNSUPPORTED
+        assert lib.sd_verify_attn_workspace_size(_shape(**{field: bad}).ref) == 0
+
+
+def test_node_counts(lib):
+    assert _attn(lib, _shape((0, 65))) == native.SD_ERR_UNSUPPORTED        # N > 64
+    assert _attn(lib, _shape((0, 5, 5))) == native.SD_ERR_INVALID_ARG      # N = 0
+    assert _attn(lib, _shape((1, 5))) == native.SD_ERR_INVALID_ARG         # indptr[0] != 0
+    s = _shape()
+    s.c.batch = 0
+    assert _attn(lib, s) == native.SD_ERR_INVALID_ARG
+    s.c.batch = native.MAX_BATCH + 1
+    assert _attn(lib, s) == native.SD_ERR_INVALID_ARG
+
+
+def test_null_pointers_and_workspace(lib):
+    assert _attn(lib, _shape(), q=None) == native.SD_ERR_INVALID_ARG
+    big = _shape((0, 23), max_pages=2050, pool=2050)
+    need = lib.sd_verify_attn_workspace_size(big.ref)
+    assert need > 0
+    assert _attn(lib, big, ws=None, ws_bytes=0) == native.SD_ERR_WORKSPACE
+    assert _attn(lib, big, ws=FAKE, ws_bytes=need - 1) == native.SD_ERR_WORKSPACE
+
+
+def test_workspace_grows_with_context_and_nodes(lib):
+    a = lib.sd_verify_attn_workspace_size(_shape((0, 9), max_pages=257, pool=257).ref)
+    b = lib.sd_verify_attn_workspace_size(_shape((0, 23), max_pages=8194, pool=8194).ref)
+    assert b > a
+
+
+def test_accept_host_checks(lib):
+    ind = (ctypes.c_int * 2)(0, 23)
+    need = lib.sd_accept_workspace_size(1, ind, 151936)
+    assert need >= 23 * 38 * 8
+    call = lambda vocab, max_path, ws, ws_bytes, logits=FAKE: lib.sd_accept(
+        1, ind, vocab, logits, FAKE, FAKE, FAKE, FAKE, FAKE, None, max_path, ws, ws_bytes, None, None)
+    assert call(0, 17, FAKE, need) == native.SD_ERR_INVALID_ARG
+    assert call(151936, 0, FAKE, need) == native.SD_ERR_INVALID_ARG
+    assert call(151936, 17, FAKE, need, logits=None) == native.SD_ERR_INVALID_ARG
+    assert call(151936, 17, FAKE, need - 1) == native.SD_ERR_WORKSPACE
+    assert call(151936, 17, None, 0) == native.SD_ERR_WORKSPACE
+
+
+def test_commit_host_checks(lib):
+    s = _shape()
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    nul = (ctypes.c_void_p * 2)(FAKE, None)
+    call = lambda layers, k=arr, new=None, ctx=FAKE: lib.sd_kv_commit(
+        s.ref, layers, k, arr, arr, arr, FAKE, ctx, new, FAKE, FAKE, 8, None, None)
+    assert call(0) == native.SD_ERR_INVALID_ARG
+    assert call(native.MAX_LAYERS + 1) == native.SD_ERR_UNSUPPORTED
+    assert call(2, k=nul) == native.SD_ERR_INVALID_ARG
+    assert call(2, new=FAKE, ctx=FAKE) == native.SD_ERR_INVALID_ARG   # new_ctx_lens aliases ctx_lens

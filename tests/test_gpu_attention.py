@@ -1,0 +1,96 @@
+"""GPU verify attention (through the C ABI) against the fp64 oracle.
+
+Element by element on small cases that still span several KV tiles and
+splits with ragged tails; sampled (row, head) outputs at the five workloads'
+full sizes in the launch configuration the bench uses; and the invariance
+of the result under the number of splits.
+"""
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_verify_decode_gb300 import synth
+
+from gpu_helpers import (check_attention, ensure_built, gpu_attention, oracle_attention, workload, f64,
+                         attn_bound)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    ensure_built()
+
+
+def _tree(seed, budget):
+    return synth.ddtree_parents(np.random.default_rng(seed), budget)[0]
+
+
+CASES = {
+    # name: (parents per sequence, ctx per sequence, qkv scale, forced splits)
+    "chain4_ctx512_auto": ([synth.chain_parents(4)], [512], 1 / 16, 0),
+    "chain8_ctx1000_one_split": ([synth.chain_parents(8)], [1000], 1.0, 1),
+    "chain8_ctx1000_three_splits": ([synth.chain_parents(8)], [1000], 1.0, 3),
+    "tree22_ctx3000_five_splits": ([_tree(1, 22)], [3000], 1.0, 5),
+    "tree22_ctx3000_auto_spiky": ([_tree(2, 22)], [3000], 3.0, 0),
+    "ragged_batch_mixed_trees": ([synth.chain_parents(0), synth.chain_parents(4), _tree(3, 22),
+                                  synth.chain_parents(8), _tree(4, 63)], [0, 1, 17, 700, 2049], 1.0, 0),
+    "max_nodes64_ctx300": ([_tree(5, 63)], [300], 1.0, 2),
+    "empty_context_tree": ([_tree(6, 22)], [0], 1.0, 0),
+    "ctx_one_page_exact": ([synth.chain_parents(4), synth.chain_parents(4)], [16, 64], 0.5, 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_attention_matches_oracle(name):
+    parents, ctx, scale, splits = CASES[name]
+    w = workload(parents, ctx, seed=len(name), scale=scale)
+    out, lse, status = gpu_attention(w, 0, num_splits=splits)
+    assert status == 0
+    ref, ref_lse = oracle_attention(w, 0)
+    check_attention(out, ref, lse, ref_lse)
+
+
+def test_tiny_chain_workload_full():
+    w = synth.make_workload("tiny_chain_ctx512", device="cuda")
+    out, lse, status = gpu_attention(w, 0)
+    assert status == 0
+    ref, ref_lse = oracle_attention(w, 0)
+    check_attention(out, ref, lse, ref_lse)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+def test_split_count_invariance(splits):
+    w = workload([_tree(7, 22)], [2500], seed=77, scale=1.0)
+    base, base_lse, _ = gpu_attention(w, 0, num_splits=1)
+    out, lse, status = gpu_attention(w, 0, num_splits=splits)
+    assert status == 0
+    ref = f64(base)
+    assert float(np.abs(f64(out) - ref).max()) <= 1e-2 * float(np.abs(ref).max()) + 1e-6
+    assert float(np.abs(f64(lse) - f64(base_lse)).max()) <= 1e-4
+
+
+FULL = ["chain8_ctx4k", "ddtree22_ctx32k", "conc8_chain4_ragged", "ddtree22_ctx128k"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full-size shapes, bench launch configuration, sampled outputs vs the oracle."""
+    w = synth.make_workload(name, device="cuda", layers=1, logits=False)
+    out, lse, status = gpu_attention(w, 0)
+    assert status == 0
+    got = f64(out)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(5)
+    n = w.total_nodes
+    rows = sorted(set([0, n - 1] + list(rng.integers(0, n, size=10))))
+    samples = [(int(r), int(h)) for r in rows for h in (0, 5, 6, 13, 23)]
+    ref, ref_lse = oracle_attention(w, 0, samples=samples)
+    sub = np.stack([got[r, h] for r, h in samples])
+    err = float(np.abs(sub - ref).max())
+    assert err <= attn_bound(ref)
+    assert err <= 1e-2 * float(np.abs(ref).max()) + 1e-6, err
+    sub_lse = np.array([f64(lse)[r, h] for r, h in samples])
+    assert float(np.abs(sub_lse - ref_lse).max()) <= 2e-4 + 1e-4 * float(np.abs(ref_lse).max())
