@@ -164,7 +164,8 @@ def run_ours(args, world, rank, local):
     native.load()
     w = synth.make_workload(args.config, device=dev)
     d = device_inputs(w, dev)
-    step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev)
+    step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev,
+                      num_splits=args.splits)
     run_args = (w.q, w.k_cache, w.v_cache, w.k_new, w.v_new, d["page_table"], d["ctx_lens"], d["parents"],
                 d["draft_tokens"], w.logits)
     step.run(*run_args)                       # eager once: surfaces launch errors early
@@ -329,6 +330,7 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0, help="split-KV chunks per (sequence, KV head); 0 = auto")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

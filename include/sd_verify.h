@@ -37,7 +37,7 @@
  *    N_b = q_indptr[b+1]-q_indptr[b] must be 1..64.  Node 0 of a sequence is
  *    the root: the last token already emitted, whose K/V is not cached yet.
  *    parents[] holds per-sequence local ids: parents[root] = -1 and
- *    0 <= parents[j] < j otherwise (a chain is 0,1,..,N-2 shifted: -1,0,1,..).
+ *    0 <= parents[j] < j otherwise (a chain of N nodes is -1, 0, 1, .., N-2).
  *  - The KV cache of one layer is [num_pool_pages][4][16][256] bf16
  *    (page-major, then KV head, then slot, then dim).  page_table is
  *    [B][max_pages_per_seq] int32; context token p of sequence b lives in
@@ -76,6 +76,7 @@ typedef enum {
 #define SD_DEV_BAD_ACCEPT    8   /* accept_len / path out of range at commit time */
 #define SD_DEV_NAN_LOGITS   16   /* a logits row holds NaN (argmax of such a row is unspecified) */
 #define SD_DEV_PATH_OVERFLOW 32  /* accept length larger than max_path */
+#define SD_DEV_TIMEOUT      64   /* an internal pipeline wait expired (about 1 s); outputs unspecified */
 
 #define SD_MAX_BATCH 256
 #define SD_MAX_NODES 64

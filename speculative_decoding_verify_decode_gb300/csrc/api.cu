@@ -3,6 +3,7 @@
 // here allocates device memory or synchronises; every launch goes on the
 // caller's stream.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -50,21 +51,30 @@ int device_sm_count() {
   return sms;
 }
 
+// Which attention kernel runs: the mma.sync kernel unless SDV_ATTN_IMPL=tc.
+bool use_tc() {
+  const char* e = std::getenv("SDV_ATTN_IMPL");
+  return e != nullptr && std::strcmp(e, "tc") == 0;
+}
+
 struct SplitPlan {
   int chunk;     // context tokens per split
   int nsplit;    // splits in the grid
 };
 
-// Context tokens per split: enough CTAs for about two per SM, but at least
-// four context tokens per query row so that the partial outputs (1 KB per
-// row) stay well below the K/V bytes the split reads (1 KB per token).
+// Context tokens per split: about one CTA per SM (two for the mma.sync
+// kernel), but at least four context tokens per query row so that the
+// partial outputs (1 KB per row) stay well below the K/V bytes the split
+// reads (1 KB per token).
 SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
-  const int tile = attn_mma_tile();
+  const bool tc = use_tc();
+  const int tile = tc ? attn_tc_tile() : attn_mma_tile();
   const long long max_ctx = (long long)s->max_pages_per_seq * kPage;
   long long want = s->num_splits;
   if (want == 0) {
-    const int ctas = attn_mma_ctas_per_split(bd);
-    want = (2LL * device_sm_count() + ctas - 1) / ctas;
+    const int ctas = tc ? bd.batch * kHkv * tc_plan(bd.max_nodes).hparts : attn_mma_ctas_per_split(bd);
+    const int per_sm = tc ? 1 : 2;
+    want = ((long long)per_sm * device_sm_count() + ctas - 1) / ctas;
   }
   long long chunk = (max_ctx + want - 1) / want;
   if (s->num_splits == 0) {
@@ -142,7 +152,8 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(float)));
   }
-  return cuda_status(launch_attn_mma(p, bd, static_cast<cudaStream_t>(stream)));
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return cuda_status(use_tc() ? launch_attn_tc(p, bd, cs) : launch_attn_mma(p, bd, cs));
 }
 
 size_t sd_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {

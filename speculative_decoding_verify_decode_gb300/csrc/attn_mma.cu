@@ -304,42 +304,6 @@ attn_split_mma_kernel(const AttnParams p, const BatchDesc bd) {
   }
 }
 
-// One warp per (node row, query head): combine the active splits.
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const BatchDesc bd) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 8 + warp;
-  if (pair >= bd.total_nodes * kHq) return;
-  const int r = pair / kHq, head = pair % kHq;
-  int b = 0;
-  while (b + 1 < bd.batch && bd.q_indptr[b + 1] <= r) ++b;
-  int L = p.ctx_lens[b];
-  L = L < 0 ? 0 : min(L, p.max_pages * kPage);
-  const int ns = active_splits(L, p.chunk);
-  if (ns == 1) return;  // written directly by the split kernel
-  float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, p.lse_part[((size_t)s * bd.total_nodes + r) * kHq + head]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const size_t row = ((size_t)s * bd.total_nodes + r) * kHq + head;
-    const float w = fast_exp2(p.lse_part[row] - mx);
-    den += w;
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + row * kDim + lane * 8);
-    const float4 a = src[0], c = src[1];
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
-  }
-  const float inv = 1.f / den;
-  __nv_bfloat16* dst = p.out + ((size_t)r * kHq + head) * kDim + lane * 8;
-  uint4 packed;
-  packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(dst) = packed;
-  if (p.lse != nullptr && lane == 0) p.lse[(size_t)r * kHq + head] = (mx + fast_log2(den)) * kLn2;
-}
-
 template <int NW>
 cudaError_t launch_split(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   constexpr int R = 16 * NW;
@@ -370,9 +334,7 @@ cudaError_t launch_attn_mma(const AttnParams& p, const BatchDesc& bd, cudaStream
   else if (M <= 64) e = launch_split<4>(p, bd, st);
   else e = launch_split<9>(p, bd, st);
   if (e != cudaSuccess || p.num_splits == 1) return e;
-  const int pairs = bd.total_nodes * kHq;
-  attn_merge_kernel<<<(pairs + 7) / 8, 256, 0, st>>>(p, bd);
-  return cudaGetLastError();
+  return launch_attn_merge(p, bd, st);
 }
 
 }  // namespace sdv

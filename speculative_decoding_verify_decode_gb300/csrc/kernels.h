@@ -10,6 +10,21 @@ int attn_mma_tile();
 int attn_mma_ctas_per_split(const BatchDesc& bd);
 cudaError_t launch_attn_mma(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 
+// Verify attention on tcgen05 tiles with TMA-staged pages (+ merge when num_splits > 1).
+constexpr int kTcMaxNQ = 112;   // query columns per CTA (heads-per-CTA x nodes, padded to 16)
+struct TcPlan {
+  int hpc;      // query heads of a KV group handled by one CTA: 6, 3, 2 or 1
+  int hparts;   // CTAs per (split, KV head): ceil(6 / hpc)
+  int nq;       // query columns per CTA: hpc x max nodes rounded up to 16 (>= 32)
+};
+TcPlan tc_plan(int max_nodes);
+size_t tc_smem_bytes(int nq);
+int attn_tc_tile();
+cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+
+// Log-sum-exp merge of the split partials into the bf16 output.
+cudaError_t launch_attn_merge(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+
 // Argmax + greedy path selection.
 struct AcceptParams {
   const float* logits;

@@ -24,6 +24,7 @@ SD_DEV_BAD_CTX = 4
 SD_DEV_BAD_ACCEPT = 8
 SD_DEV_NAN_LOGITS = 16
 SD_DEV_PATH_OVERFLOW = 32
+SD_DEV_TIMEOUT = 64
 MAX_NODES = 64
 MAX_BATCH = 256
 MAX_LAYERS = 64
