@@ -163,6 +163,8 @@ def plant_drafts(rng: np.random.Generator, parents: np.ndarray, tau: np.ndarray,
         if planted[j] and target not in sib and rng.random() < p_accept:
             tok = target
         else:
+            if vocab - 1 - len(sib - {target}) <= 0:
+                raise ValueError("vocabulary too small for distinct rejected sibling drafts")
             while True:
                 tok = int(rng.integers(vocab))
                 if tok != target and tok not in sib:

@@ -55,7 +55,7 @@ def test_accept_on_workloads(name):
     _check_accept(w, w.logits, st)
 
 
-@pytest.mark.parametrize("vocab", [151936, 4096, 1001, 1])
+@pytest.mark.parametrize("vocab", [151936, 4096, 1001, 64])
 def test_accept_unplanted_normal_logits(vocab):
     rng = np.random.default_rng(vocab)
     parents = [synth.ddtree_parents(rng, 22)[0], synth.chain_parents(8), synth.chain_parents(0)]
@@ -68,6 +68,15 @@ def test_accept_unplanted_normal_logits(vocab):
         w.draft_tokens[lo:hi] = synth.plant_drafts(rng, w.parents[lo:hi], t[lo:hi], vocab, 0.8)
     st = _run_accept(w, logits)
     _check_accept(w, logits, st)
+
+
+def test_vocab_of_one_accepts_every_draft():
+    w = workload([synth.chain_parents(6)], [16], seed=5, vocab=1, p=1.0, logits=False)
+    w.draft_tokens = np.zeros(7, dtype=np.int32)
+    logits = torch.randn((7, 1), device="cuda")
+    st = _run_accept(w, logits)
+    lens = _check_accept(w, logits, st)
+    assert lens[0] == 7
 
 
 def test_argmax_ties_across_chunks_and_signed_zero():
