@@ -76,25 +76,37 @@ __global__ void __launch_bounds__(256) argmax_chunk_kernel(const AcceptParams p)
   }
 }
 
-__global__ void __launch_bounds__(kMaxNodes) accept_kernel(const AcceptParams p, const BatchDesc bd) {
+constexpr int kAcceptThreads = 256;
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptParams p, const BatchDesc bd) {
   const int b = blockIdx.x;
   const int q0 = bd.q_indptr[b];
   const int n = bd.q_indptr[b + 1] - q0;
   const int j = threadIdx.x;
+  const int warp = j >> 5, lane = j & 31;
   __shared__ int s_t[kMaxNodes], s_par[kMaxNodes], s_depth[kMaxNodes], s_acc[kMaxNodes];
   __shared__ int s_bad;
   if (j == 0) s_bad = 0;
-  if (j < n) {
-    const ValIdx* part = reinterpret_cast<const ValIdx*>(p.partial) + (size_t)(q0 + j) * p.chunks;
-    float bv = part[0].v;
-    int bi = part[0].i;
-    for (int c = 1; c < p.chunks; ++c)
+  // Finish each row's argmax: one warp per row, lanes across the row's chunks.
+  for (int row = warp; row < n; row += kAcceptThreads / 32) {
+    const ValIdx* part = reinterpret_cast<const ValIdx*>(p.partial) + (size_t)(q0 + row) * p.chunks;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int c = lane; c < p.chunks; c += 32)
       if (beats(part[c].v, part[c].i, bv, bi)) { bv = part[c].v; bi = part[c].i; }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
     if (bi == INT_MAX) bi = 0;  // unreachable for finite rows; keeps the token in range
-    s_t[j] = bi;
-    s_par[j] = p.parents[q0 + j];
-    if (p.target_tokens != nullptr) p.target_tokens[q0 + j] = bi;
+    if (lane == 0) {
+      s_t[row] = bi;
+      if (p.target_tokens != nullptr) p.target_tokens[q0 + row] = bi;
+    }
   }
+  if (j < n) s_par[j] = p.parents[q0 + j];
   __syncthreads();
   if (j < n) {
     // Walk the root path of j: depth, validity, and whether every node on it
@@ -149,11 +161,12 @@ __global__ void __launch_bounds__(kMaxNodes) accept_kernel(const AcceptParams p,
 
 cudaError_t launch_accept(const AcceptParams& p, const BatchDesc& bd, cudaStream_t st) {
   dim3 grid(p.chunks, bd.total_nodes);
-  if (p.vocab % 4 == 0) argmax_chunk_kernel<true><<<grid, 256, 0, st>>>(p);
+  const bool aligned = (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
+  if (p.vocab % 4 == 0 && aligned) argmax_chunk_kernel<true><<<grid, 256, 0, st>>>(p);
   else argmax_chunk_kernel<false><<<grid, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  accept_kernel<<<bd.batch, kMaxNodes, 0, st>>>(p, bd);
+  accept_kernel<<<bd.batch, kAcceptThreads, 0, st>>>(p, bd);
   return cudaGetLastError();
 }
 

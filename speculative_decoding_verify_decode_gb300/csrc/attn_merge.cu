@@ -16,11 +16,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// One warp per (node row, query head): combine the active splits.
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const BatchDesc bd) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 8 + warp;
-  if (pair >= bd.total_nodes * kHq) return;
+// One 64-thread block per (node row, query head).  Thread t owns dims
+// 4t..4t+3; the split weights come from a block-wide max of the split LSEs.
+constexpr int kMergeThreads = 64;
+
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p, const BatchDesc bd) {
+  const int pair = blockIdx.x;
   const int r = pair / kHq, head = pair % kHq;
   int b = 0;
   while (b + 1 < bd.batch && bd.q_indptr[b + 1] <= r) ++b;
@@ -28,35 +29,55 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   L = L < 0 ? 0 : min(L, p.max_pages * kPage);
   const int ns = active_splits(L, p.chunk);
   if (ns == 1) return;  // written directly by the split kernel
+  const size_t stride = (size_t)bd.total_nodes * kHq;   // rows between splits
+  const size_t row0 = (size_t)r * kHq + head;
+  __shared__ float s_red[kMergeThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, p.lse_part[((size_t)s * bd.total_nodes + r) * kHq + head]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = tid; s < ns; s += kMergeThreads) mx = fmaxf(mx, p.lse_part[s * stride + row0]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(s_red[0], s_red[1]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const size_t row = ((size_t)s * bd.total_nodes + r) * kHq + head;
-    const float w = fast_exp2(p.lse_part[row] - mx);
-    den += w;
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + row * kDim + lane * 8);
-    const float4 a = src[0], c = src[1];
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+  int s = 0;
+  for (; s + 4 <= ns; s += 4) {
+    float w[4];
+    float4 o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t row = (s + k) * stride + row0;
+      w[k] = p.lse_part[row];
+      o[k] = reinterpret_cast<const float4*>(p.o_part + row * kDim)[tid];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float wk = fast_exp2(w[k] - mx);
+      den += wk;
+      acc.x += wk * o[k].x; acc.y += wk * o[k].y; acc.z += wk * o[k].z; acc.w += wk * o[k].w;
+    }
+  }
+  for (; s < ns; ++s) {
+    const size_t row = s * stride + row0;
+    const float wk = fast_exp2(p.lse_part[row] - mx);
+    const float4 o = reinterpret_cast<const float4*>(p.o_part + row * kDim)[tid];
+    den += wk;
+    acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
   }
   const float inv = 1.f / den;
-  __nv_bfloat16* dst = p.out + ((size_t)r * kHq + head) * kDim + lane * 8;
-  uint4 packed;
-  packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(dst) = packed;
-  if (p.lse != nullptr && lane == 0) p.lse[(size_t)r * kHq + head] = (mx + fast_log2(den)) * kLn2;
+  uint2 packed;
+  packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(p.out + row0 * kDim)[tid] = packed;
+  if (p.lse != nullptr && tid == 0) p.lse[row0] = (mx + fast_log2(den)) * kLn2;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_merge(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
-  const int pairs = bd.total_nodes * kHq;
-  attn_merge_kernel<<<(pairs + 7) / 8, 256, 0, st>>>(p, bd);
+  attn_merge_kernel<<<bd.total_nodes * kHq, kMergeThreads, 0, st>>>(p, bd);
   return cudaGetLastError();
 }
 
