@@ -33,7 +33,7 @@ from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inp
 
 METRIC = "verify steps/s"
 DEFAULT_CONFIG = "chain8_ctx4k"
-ATTN_SRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", "attn_mma.cu")
+ATTN_SRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", "attn_tc.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
 
 

@@ -29,6 +29,8 @@
  *    matching *_workspace_size query.  Calls are asynchronous and ordered on
  *    `stream` (a cudaStream_t passed as void*; NULL = the legacy default
  *    stream), so a whole step can be captured into one CUDA graph.
+ *  - bf16 tensors (q, caches, k_new/v_new, out) and workspaces must start on a
+ *    16-byte boundary (SD_ERR_INVALID_ARG otherwise).
  *  - Geometry is fixed: 24 query heads, 4 KV heads, head_dim 256, 16-token
  *    pages.  Query head h reads KV head h / 6.  bf16 tensors are raw 16-bit
  *    bf16 values (uint16 storage is fine).

@@ -3,7 +3,6 @@
 // here allocates device memory or synchronises; every launch goes on the
 // caller's stream.
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -51,35 +50,29 @@ int device_sm_count() {
   return sms;
 }
 
-// Which attention kernel runs: the mma.sync kernel unless SDV_ATTN_IMPL=tc.
-bool use_tc() {
-  const char* e = std::getenv("SDV_ATTN_IMPL");
-  return e != nullptr && std::strcmp(e, "tc") == 0;
-}
-
 struct SplitPlan {
   int chunk;     // context tokens per split
   int nsplit;    // splits in the grid
 };
 
-// Context tokens per split: about one CTA per SM (two for the mma.sync
-// kernel), but at least four context tokens per query row so that the
-// partial outputs (1 KB per row) stay well below the K/V bytes the split
-// reads (1 KB per token).
+// Context tokens per split.  Every split CTA (one per SM) pays a fixed
+// set-up and epilogue, so a single sequence gets one wave of CTAs, each with
+// an equal share of the 128-token tiles; a batch, whose context lengths are
+// not known on the host, is cut for two waves of the worst case (every
+// sequence full), which keeps the last wave short when the lengths are ragged.
 SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
-  const bool tc = use_tc();
-  const int tile = tc ? attn_tc_tile() : attn_mma_tile();
+  const int tile = attn_tc_tile();
   const long long max_ctx = (long long)s->max_pages_per_seq * kPage;
-  long long want = s->num_splits;
-  if (want == 0) {
-    const int ctas = tc ? bd.batch * kHkv * tc_plan(bd.max_nodes).hparts : attn_mma_ctas_per_split(bd);
-    const int per_sm = tc ? 1 : 2;
-    want = ((long long)per_sm * device_sm_count() + ctas - 1) / ctas;
-  }
-  long long chunk = (max_ctx + want - 1) / want;
-  if (s->num_splits == 0) {
-    const long long min_chunk = 4LL * bd.max_nodes * kGroup;
-    if (chunk < min_chunk) chunk = min_chunk;
+  const long long max_tiles = (max_ctx + tile - 1) / tile;
+  long long chunk;
+  if (s->num_splits > 0) {
+    chunk = (max_ctx + s->num_splits - 1) / s->num_splits;
+  } else {
+    const long long streams = (long long)bd.batch * kHkv * tc_plan(bd.max_nodes).hparts;
+    const long long waves = bd.batch > 1 ? 2 : 1;
+    const long long slots = waves * device_sm_count();
+    const long long per_cta = (streams * max_tiles + slots - 1) / slots;
+    chunk = (per_cta < 1 ? 1 : per_cta) * tile;
   }
   chunk = (chunk + tile - 1) / tile * tile;
   if (chunk < tile) chunk = tile;
@@ -95,6 +88,9 @@ size_t attn_workspace(const SplitPlan& pl, const BatchDesc& bd) {
 }
 
 sd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SD_OK : SD_ERR_CUDA; }
+
+// The kernels move bf16 rows with 16-byte vector accesses.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -126,6 +122,9 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
   if (st != SD_OK) return st;
   if (!q || !k_cache || !v_cache || !k_new || !v_new || !page_table || !ctx_lens || !parents || !out)
     return SD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
+    return SD_ERR_INVALID_ARG;
   const SplitPlan pl = plan_splits(shape, bd);
   const size_t need = attn_workspace(pl, bd);
   if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SD_ERR_WORKSPACE;
@@ -152,8 +151,7 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(float)));
   }
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return cuda_status(use_tc() ? launch_attn_tc(p, bd, cs) : launch_attn_mma(p, bd, cs));
+  return cuda_status(launch_attn_tc(p, bd, static_cast<cudaStream_t>(stream)));
 }
 
 size_t sd_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {
@@ -207,6 +205,9 @@ sd_status sd_kv_commit(const sd_shape* shape, int num_layers, void* const* k_cac
   std::memset(&p, 0, sizeof(p));
   for (int l = 0; l < num_layers; ++l) {
     if (!k_cache_layers[l] || !v_cache_layers[l] || !k_new_layers[l] || !v_new_layers[l])
+      return SD_ERR_INVALID_ARG;
+    if (!aligned16(k_cache_layers[l]) || !aligned16(v_cache_layers[l]) || !aligned16(k_new_layers[l]) ||
+        !aligned16(v_new_layers[l]))
       return SD_ERR_INVALID_ARG;
     p.k_cache[l] = k_cache_layers[l];
     p.v_cache[l] = v_cache_layers[l];

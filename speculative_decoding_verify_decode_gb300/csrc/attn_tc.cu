@@ -11,25 +11,34 @@
 // 16-token pages from one pool; §5.3: bottom-right causal mask of a chain).
 //
 // Layout of the work.  A CTA owns (split s, KV head g, head part c, sequence
-// b): hpc query heads of group g (6, 3, 2 or 1, so that hpc * N <= 112)
+// b): hpc query heads of group g (6, 3, 2 or 1, so that hpc * N <= 96)
 // times the sequence's N draft nodes form NQ (multiple of 16) query columns.
 // Tokens are the MMA's M dimension ("swap-AB"), so a 128-token K/V tile
 // serves every query column at once:
-//   S^T[128 tok][NQ]   = K_tile[128 tok][256]  . Q^T          (K-major A and B)
-//   O^T[256 dim][NQ]  += V_tile^T[256][128 tok] . P^T[128][NQ]  (MN-major A and B)
-// S^T (double-buffered) and O^T live in tensor memory: 4 * NQ <= 448 of the
-// 512 columns.  When a sequence needs several CTAs for its query heads (hpc
-// < 6), the CTAs of one split are adjacent in launch order and read the same
-// pages while they are still in L2.
+//   S^T[128 tok][NQ]  = K_tile[128 tok][256] . Q^T                (K-major A and B)
+//   O^T[256 dim][NQ] += V_tile^T[256][128 tok] . P^T[128 tok][NQ]  (MN-major A and B)
+//   l[NQ]            += 1^T . P^T                                  (column sums of P)
+// S^T (double-buffered), O^T and l live in tensor memory (5 * NQ <= 480 of
+// the 512 columns).  The column sums are taken by the tensor core from the
+// same bf16 P^T the PV product uses.  When a sequence needs several CTAs for
+// its query heads (hpc < 6), the CTAs of one split are adjacent in launch
+// order and read the same pages while they are still in L2.
 //
-// Warp roles (192 threads): warp 0 streams K/V pages with TMA (16 tokens x
-// 64 dims per box, 128-byte swizzle), warp 1 allocates tensor memory and one
-// lane issues every tcgen05.mma, warps 2-5 (one per tensor-memory lane
-// quarter, thread = token row) run the online softmax: masking, a running
-// per-column maximum that is only raised (and O^T rescaled) when a score
-// exceeds it by more than 2^8, exp2, column sums by a warp transpose-reduce,
-// and the bf16 P^T tile for the PV product.  Every wait on an mbarrier is
-// bounded; on expiry the kernel reports SD_DEV_TIMEOUT and winds down.
+// Operand tiles (Q^T, K, V) are "block-major": four 64-dim blocks, each
+// holding every row of the tile at 128 B with the 128-byte swizzle, so the
+// UMMA descriptors step 1 KB between 8-row groups.  A TMA box of 16 rows x 64
+// dims (one page of one KV head, one block) writes 2 KB of a block; a
+// 128-token tile takes 32 boxes.
+//
+// Warp roles (224 threads): warp 0 streams K tiles and warp 6 V tiles with
+// TMA; warp 1 allocates tensor memory and one lane issues every tcgen05.mma,
+// taking QK of tile i and PV of tile i-1 in whichever order their inputs
+// arrive; warps 2-5 (one per tensor-memory lane quarter, thread = token row)
+// run the online softmax: masking, a running per-column maximum that is only
+// raised (and O^T, l rescaled) when a score exceeds it by more than 2^8,
+// exp2, and the bf16 P^T tile.  Every wait on an mbarrier is bounded; on
+// expiry the kernel reports SD_DEV_TIMEOUT and winds down.
+#include <cstddef>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -39,25 +48,35 @@ namespace sdv {
 namespace {
 
 constexpr int kT = 128;                 // tokens per tile
-constexpr int kRegionB = kT * 128;      // one 64-dim block of a K/V tile: 16 KB
+constexpr int kRegionB = kT * 128;      // one 64-dim block of a K/V tile: 128 rows x 128 B = 16 KB
 constexpr int kTileB = 4 * kRegionB;    // 64 KB
-constexpr int kThreads = 192;
+constexpr int kOnesB = 1024;            // the all-ones operand: 8 rows x 128 B
+constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
+constexpr int kThreads = 224;
+constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 
 enum Bar { K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE, GROUP, NUM_BARS };
 
+constexpr int kCols = 128;   // per-column arrays padded to whole 32-column groups
+
+// Per-column arrays first: each is read with 16-byte vector loads.
 struct Small {
+  float m[kCols];
+  float alpha[kCols];
+  float red[4][kCols];
+  int colnode[kCols];
   uint64_t bar[NUM_BARS];
   uint64_t anc[kMaxNodes];
-  float m[kTcMaxNQ];
-  float alpha[kTcMaxNQ];
-  float red[4][kTcMaxNQ];
-  int colnode[kTcMaxNQ];
   int flag[2][4];
   uint32_t tmem;
   int abort;
 };
+static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &&
+                  offsetof(Small, red) % 16 == 0 && offsetof(Small, colnode) % 16 == 0,
+              "per-column arrays must be 16-byte aligned");
+static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -76,10 +95,22 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+// Test a phase; the waiting thread is suspended in hardware (up to about
+// 10 ms, or until the phase completes) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(10000000u)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
@@ -87,7 +118,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait: false (and the CTA's abort flag set) if the phase never completes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Small* sm, int* status) {
-  if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
@@ -158,25 +188,57 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 
-// Byte offset of 16-byte chunk cc (0..7) of row r inside a 128-byte-swizzled
-// block whose rows are 128 bytes apart (8-row groups 1024 bytes apart).
-__device__ __forceinline__ uint32_t sw_off(int r, int cc) {
+// Byte offset of 16-byte chunk c (0..31) of row r in a group-major operand
+// tile: group r/8, 64-dim block c/8, row r%8, swizzled chunk (c%8) ^ (r%8).
+__device__ __forceinline__ uint32_t tile_off(int rows, int r, int c) {
+  return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// Byte offset of 16-byte chunk cc (0..7) of token row r in the P^T tile
+// (MN-major: 64-column atoms of 128 rows x 128 B, 128-byte swizzle).
+__device__ __forceinline__ uint32_t p_off(int r, int cc) {
   return (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
 }
 
-// Copy one 512-byte row (256 bf16) into a K-major tile of `rows_per_block`
-// rows per 64-dim block, or zero it when src is null.  One lane moves 16 B.
-__device__ __forceinline__ void put_row_chunk(uint8_t* base, int rows_per_block, int r, int c,
-                                              const __nv_bfloat16* src) {
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (src != nullptr) v = *reinterpret_cast<const uint4*>(src + c * 8);
-  *reinterpret_cast<uint4*>(base + (c >> 3) * rows_per_block * 128 + sw_off(r, c & 7)) = v;
+// Copy `nrows` rows of 256 bf16 into a group-major tile (row r's source is
+// src_of(r), or zeros when that is null).  `nthreads` threads starting at `t`
+// share the work; each keeps 8 independent 16-byte loads in flight.
+template <typename SrcFn>
+__device__ __forceinline__ void stage_rows(uint8_t* base, int rows, int r0, int nrows, SrcFn src_of, int t,
+                                           int nthreads) {
+  constexpr int U = 8;
+  const int tasks = nrows * 32;
+  for (int t0 = t; t0 < tasks; t0 += nthreads * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int task = t0 + u * nthreads;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (task < tasks) {
+        const __nv_bfloat16* src = src_of(task >> 5);
+        if (src != nullptr) v[u] = __ldg(reinterpret_cast<const uint4*>(src) + (task & 31));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int task = t0 + u * nthreads;
+      if (task < tasks) *reinterpret_cast<uint4*>(base + tile_off(rows, r0 + (task >> 5), task & 31)) = v[u];
+    }
+  }
+}
+
+// Element g of a small per-thread array, by a select chain rather than a
+// dynamically indexed (local-memory) access.
+template <int N>
+__device__ __forceinline__ uint32_t vis_of(const uint32_t (&a)[N], int g) {
+  uint32_t r = a[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) r = (g == k) ? a[k] : r;
+  return r;
 }
 
 // Reduce 32 values per lane across the warp so that lane L ends with the
-// sum (or max) over all lanes of value L (transpose-reduce, 31 shuffles).
-template <bool kMax>
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+// maximum over all lanes of value L (transpose-reduce, 31 shuffles).
+__device__ __forceinline__ float transpose_max32(float (&v)[32], int lane) {
 #pragma unroll
   for (int half = 16; half >= 1; half >>= 1) {
     const bool up = (lane & half) != 0;
@@ -184,8 +246,7 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
     for (int i = 0; i < half; ++i) {
       const float send = up ? v[i] : v[i + half];
       const float keep = up ? v[i + half] : v[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, half);
-      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
     }
   }
   return v[0];
@@ -197,14 +258,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
   constexpr int NG = (NQ + 31) / 32;          // 32-column groups
   constexpr int NATOM = (NQ + 63) / 64;       // 64-column atoms of the P^T tile
-  constexpr int kQB = NQ * 512;               // Q^T: 4 blocks of NQ rows x 128 B
-  extern __shared__ uint8_t dyn_smem[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
+  constexpr int kQB = NQ * 512;               // Q^T tile: 4 blocks of NQ rows x 128 B
+  constexpr uint32_t kColS0 = 0, kColO = 2 * NQ, kColL = 4 * NQ;   // tensor-memory columns
+  static_assert(5 * NQ <= 512, "tensor memory holds 2 S^T, 2 O^T halves and l");
+  // The kernel declares no static shared memory, so the dynamic window starts
+  // at a 1024-byte boundary (required by the 128-byte swizzle atoms); indexing
+  // it directly keeps every access a shared-space one.
+  extern __shared__ __align__(1024) uint8_t dyn_smem[];
+  uint8_t* sQ = dyn_smem;
   uint8_t* sK = sQ + kQB;
   uint8_t* sV = sK + kTileB;
   uint8_t* sP = sV + kTileB;
-  Small* sm = reinterpret_cast<Small*>(sP + NATOM * kRegionB);
+  uint8_t* sOnes = sP + NATOM * kAtomB;       // 1 KB of bf16 1.0: the all-ones operand
+  Small* sm = reinterpret_cast<Small*>(sOnes + kOnesB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bid = blockIdx.x;
@@ -229,6 +295,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_ctx_tiles = ctx_end > ctx_begin ? (ctx_end - ctx_begin + kT - 1) / kT : 0;
   const int n_tiles = n_ctx_tiles + (has_draft ? 1 : 0);
   const int head0 = g * kGroup + c * hpc;
+  if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
+    if (threadIdx.x == 0) report(p.dev_status, SD_DEV_TIMEOUT);
+    return;
+  }
 
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
@@ -239,10 +309,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     sm->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int q = tid; q < NQ; q += kThreads) {
-    sm->m[q] = -INFINITY;
+  for (int q = tid; q < kCols; q += kThreads) {
+    sm->m[q] = q < NQ ? -INFINITY : 0.f;
     sm->colnode[q] = q < rows ? q / hpc : -1;
   }
+  for (int i = tid; i < kOnesB / 16; i += kThreads)   // bf16 1.0 = 0x3F80
+    reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   if (has_draft && tid < n_nodes) {
     // ancestor bitmask of node tid (bit i: i is tid or an ancestor of tid)
     uint64_t mask = 1ull << tid;
@@ -261,37 +333,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); mask = 1ull << tid; }
     sm->anc[tid] = mask;
   }
-  // Q^T (K-major): column q = node * hpc + head-in-part; zero columns past `rows`.
-  for (int task = tid; task < NQ * 32; task += kThreads) {
-    const int q = task >> 5, ch = task & 31;
-    const __nv_bfloat16* src = nullptr;
-    if (q < rows) src = p.q + ((size_t)(q0 + q / hpc) * kHq + head0 + q % hpc) * kDim;
-    put_row_chunk(sQ, NQ, q, ch, src);
-  }
-  if (has_draft) {  // the draft block is tile 0 of split 0: node t is token row t
-    for (int task = tid; task < kT * 32; task += kThreads) {
-      const int t = task >> 5, ch = task & 31;
-      const bool valid = t < n_nodes;
-      const size_t off = ((size_t)(q0 + (valid ? t : 0)) * kHkv + g) * kDim;
-      put_row_chunk(sK, kT, t, ch, valid ? p.k_new + off : nullptr);
-      put_row_chunk(sV, kT, t, ch, valid ? p.v_new + off : nullptr);
-    }
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm->tmem;
+  __syncthreads();  // mbarriers and per-column arrays ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    int ek = 0, ev = 0;
+  if (warp == kWarpK || warp == kWarpV) {
+    // ------------------------------------------------------------ TMA producers (K or V)
+    const bool is_k = warp == kWarpK;
+    uint8_t* dst = is_k ? sK : sV;
+    const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    const uint32_t full = bar(is_k ? K_FULL : V_FULL), empty = bar(is_k ? K_EMPTY : V_EMPTY);
     const int first = has_draft ? 1 : 0;
     const uint32_t init_full = has_draft ? 1u : 0u;
     for (int i = first; i < n_tiles; ++i) {
@@ -305,104 +357,141 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       // a page goes by TMA when it is in range and all 16 of its tokens are valid
       const bool page_full = page >= 0 && (lane + 1) * kPage <= valid;
       const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page_full);
-      for (int kv = 0; kv < 2; ++kv) {
-        uint8_t* dst = kv == 0 ? sK : sV;
-        const int e = kv == 0 ? ek++ : ev++;
-        const uint32_t parity = (uint32_t)(e & 1) ^ init_full ^ 1u;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(bar(kv == 0 ? K_EMPTY : V_EMPTY), parity, sm, p.dev_status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        // pages that are partial, missing or out of range: plain copies, zero past the context
-        for (int pi = 0; pi < 8; ++pi) {
-          if (tma_mask & (1u << pi)) continue;
-          const int pg = __shfl_sync(0xffffffffu, page, pi);
-          const __nv_bfloat16* cache = kv == 0 ? p.k_cache : p.v_cache;
-          for (int task = lane; task < kPage * 32; task += 32) {
-            const int slot = task >> 5, ch = task & 31;
-            const int tok = pi * kPage + slot;
-            const __nv_bfloat16* src = nullptr;
-            if (pg >= 0 && tok < valid) src = cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim;
-            put_row_chunk(dst, kT, tok, ch, src);
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0)
-          mbar_expect_tx(bar(kv == 0 ? K_FULL : V_FULL), (uint32_t)__popc(tma_mask) * (kPage * 512));
-        // issue the TMA boxes (page ids live in lanes 0..7)
-        for (int pi = 0; pi < 8; ++pi) {
-          const int pg = __shfl_sync(0xffffffffu, page, pi);
-          if (lane == 0 && (tma_mask & (1u << pi))) {
-            const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
-            const int y = (pg * kHkv + g) * kPage;
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk)
-              tma_load_2d(smem_u32(dst + blk * kRegionB + pi * kPage * 128), map, blk * 64, y,
-                          bar(kv == 0 ? K_FULL : V_FULL));
-          }
-        }
+      const uint32_t parity = (uint32_t)((i - first) & 1) ^ init_full ^ 1u;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+      // pages that are partial, missing or out of range: plain copies, zero past the context
+      for (int pi = 0; pi < 8; ++pi) {
+        if (tma_mask & (1u << pi)) continue;
+        const int pg = __shfl_sync(0xffffffffu, page, pi);
+        stage_rows(dst, kT, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
+          return (pg >= 0 && pi * kPage + slot < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim
+                                                        : nullptr;
+        }, lane, 32);
+      }
+      if (tma_mask != 0xffu) fence_async_smem();   // plain copies above: make them visible to the MMA
+      __syncwarp();
+      if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask) * (kPage * 512));
+      __syncwarp();
+      // lane l: page l/4, 64-dim block l%4 -- one 16-row x 64-dim box each
+      {
+        const int pi = lane >> 2, blk = lane & 3;
+        const int pg = __shfl_sync(0xffffffffu, page, pi);
+        if (tma_mask & (1u << pi))
+          tma_load_2d(smem_u32(dst + blk * kRegionB + pi * kPage * 128), map, blk * 64, (pg * kHkv + g) * kPage, full);
       }
       if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
     }
-  } else if (warp == 1) {
+  } else {
+  // ---------------------------------------------------------------- compute warps (1-5)
+  // While the producers fetch the first tiles, these five warps stage Q^T
+  // (and split 0's draft block, tile 0) and allocate tensor memory.
+  {
+    const int ct = tid - 32, nct = 5 * 32;
+    // Q^T (K-major): column q = node * hpc + head-in-part; zero columns past `rows`.
+    stage_rows(sQ, NQ, 0, NQ, [&](int q) -> const __nv_bfloat16* {
+      return q < rows ? p.q + ((size_t)(q0 + q / hpc) * kHq + head0 + q % hpc) * kDim : nullptr;
+    }, ct, nct);
+    if (has_draft) {  // the draft block is tile 0 of split 0: node t is token row t
+      stage_rows(sK, kT, 0, kT, [&](int t) -> const __nv_bfloat16* {
+        return t < n_nodes ? p.k_new + ((size_t)(q0 + t) * kHkv + g) * kDim : nullptr;
+      }, ct, nct);
+      stage_rows(sV, kT, 0, kT, [&](int t) -> const __nv_bfloat16* {
+        return t < n_nodes ? p.v_new + ((size_t)(q0 + t) * kHkv + g) * kDim : nullptr;
+      }, ct, nct);
+    }
+    if (warp == kWarpMma) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_fence_before();
+    asm volatile("bar.sync 1, 160;" ::: "memory");   // the five compute warps, all arrive unconditionally
+    tc_fence_after();
+  }
+  const uint32_t tmem = sm->tmem;
+  if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescQK = f16_idesc(128, NQ, 0, 0);
       constexpr uint32_t kIdescPV = f16_idesc(128, NQ, 1, 1);
+      constexpr uint32_t kIdescL = f16_idesc(128, NQ, 0, 1);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
+      const uint32_t ones_addr = smem_u32(sOnes);
       int kf = 0, vf = 0, pf = 0;
       int sfree[2] = {0, 0};
-      auto pv = [&](int t) -> bool {
-        if (!mbar_wait(bar(P_FULL), pf & 1, sm, p.dev_status)) return false;
-        ++pf;
-        if (!(has_draft && t == 0)) {
-          if (!mbar_wait(bar(V_FULL), vf & 1, sm, p.dev_status)) return false;
-          ++vf;
-        }
-        tc_fence_after();
+      int qk_next = 0, pv_next = 0;
+      long long idle_since = clock64();
+      while (pv_next < n_tiles) {
+        bool progressed = false;
+        // QK of the next tile: K tile landed, S^T buffer released by the softmax
+        if (qk_next < n_tiles && qk_next <= pv_next + 1) {
+          const int i = qk_next, sb = i & 1;
+          const bool k_ok = (has_draft && i == 0) || mbar_test(bar(K_FULL), kf & 1);
+          const bool s_ok = i < 2 || mbar_test(bar(S_FREE0 + sb), sfree[sb] & 1);
+          if (k_ok && s_ok) {
+            if (!(has_draft && i == 0)) ++kf;
+            if (i >= 2) ++sfree[sb];
+            tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int j = 0; j < kT / 16; ++j) {
-            // A = V^T rows 128h.., MN-major: 64-dim atoms 16 KB apart, 8-token groups 1 KB apart
-            const uint64_t a = sw128_desc(v_addr + 2 * h * kRegionB + j * 2048, kRegionB, 1024);
-            // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
-            const uint64_t bd_ = sw128_desc(p_addr + j * 2048, kRegionB, 1024);
-            umma(tmem + 2 * NQ + h * NQ, a, bd_, kIdescPV, (t > 0 || j > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kDim / 16; ++kk) {
+              // K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
+              const uint32_t off = (kk & 3) * 32;
+              umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * kRegionB + off, 16, 1024),
+                   sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024),
+                   kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(S_FULL0 + sb));
+            umma_commit(bar(K_EMPTY));
+            ++qk_next;
+            progressed = true;
           }
         }
-        umma_commit(bar(V_EMPTY));
-        umma_commit(bar(O_DONE));
-        return true;
-      };
-      bool ok = true;
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int sb = i & 1;
-        if (!(has_draft && i == 0)) {
-          if (!mbar_wait(bar(K_FULL), kf & 1, sm, p.dev_status)) break;
-          ++kf;
-        }
-        if (i >= 2) {
-          if (!mbar_wait(bar(S_FREE0 + sb), sfree[sb] & 1, sm, p.dev_status)) break;
-          ++sfree[sb];
-        }
-        tc_fence_after();
+        // PV (and the column sums) of the oldest tile whose P^T is written
+        if (pv_next < qk_next) {
+          const int t = pv_next;
+          const bool draft = has_draft && t == 0;
+          if (mbar_test(bar(P_FULL), pf & 1) && (draft || mbar_test(bar(V_FULL), vf & 1))) {
+            ++pf;
+            if (!draft) ++vf;
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kDim / 16; ++kk) {
-          // K-major: 64-dim blocks, 32 bytes per 16-element step, 8-row groups 1 KB apart
-          const uint64_t a = sw128_desc(k_addr + (kk >> 2) * kRegionB + (kk & 3) * 32, 16, 1024);
-          const uint64_t bq = sw128_desc(q_addr + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
-          umma(tmem + sb * NQ, a, bq, kIdescQK, kk > 0 ? 1u : 0u);
+            for (int j = 0; j < kT / 16; ++j) {
+              const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
+              // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
+              const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
+                umma(tmem + kColO + h * NQ, sw128_desc(v_addr + 2 * h * kRegionB + j * 2048, kRegionB, 1024),
+                     pb, kIdescPV, acc);
+              }
+              // l += 1^T . P^T: every 8-row group of the all-ones operand aliases the same 1 KB
+              umma(tmem + kColL, sw128_desc(ones_addr, 16, 0), pb, kIdescL, acc);
+            }
+            umma_commit(bar(V_EMPTY));
+            umma_commit(bar(O_DONE));
+            ++pv_next;
+            progressed = true;
+          }
         }
-        umma_commit(bar(S_FULL0 + sb));
-        umma_commit(bar(K_EMPTY));
-        if (i >= 1) ok = pv(i - 1);
+        if (progressed) {
+          idle_since = clock64();
+        } else {
+          if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
+            sm->abort = 1;
+            report(p.dev_status, SD_DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
       }
-      if (ok && !sm->abort && n_tiles > 0) pv(n_tiles - 1);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
+    // Columns are processed in groups of 32 in loops that are not unrolled;
+    // S^T is re-read from tensor memory by each pass.
     const int sw = warp - 2;                 // 0..3
     const int quarter = warp & 3;            // tensor-memory lane quarter of this warp
     const int row = quarter * 32 + lane;     // token row of S^T / dim row of O^T
@@ -414,60 +503,88 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (lane == 0) mbar_arrive(bar(GROUP));
       return mbar_wait(bar(GROUP), (uint32_t)(gphase++ & 1), sm, p.dev_status);
     };
-    float lcol[NG];
+    auto load_cols = [&](const float* arr, int col, float (&w)[32]) {
+      const float4* src = reinterpret_cast<const float4*>(arr + col);
 #pragma unroll
-    for (int i = 0; i < NG; ++i) lcol[i] = 0.f;
+      for (int k = 0; k < 8; ++k) {
+        const float4 t = src[k];
+        w[4 * k] = t.x; w[4 * k + 1] = t.y; w[4 * k + 2] = t.z; w[4 * k + 3] = t.w;
+      }
+    };
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
       if (!mbar_wait(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
       tc_fence_after();
-      float sv[NG * 32];
-#pragma unroll
-      for (int c16 = 0; c16 < NQ / 16; ++c16) {
-        float v[16];
-        tmem_ld16(tmem + lane_addr + sb * NQ + c16 * 16, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sv[c16 * 16 + e] = v[e];
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
-
-      // mask, scale, and check whether any score outgrows its column maximum
+      const uint32_t s_addr = tmem + lane_addr + kColS0 + sb * NQ;
       const bool draft_tile = has_draft && i == 0;
       const int t0 = ctx_begin + (i - (has_draft ? 1 : 0)) * kT;
       const int valid = draft_tile ? n_nodes : min(kT, ctx_end - t0);
-      bool over = false;
+      // Visibility of this thread's token row, one bit per column of each
+      // 32-column group: context rows before `valid` see every query column;
+      // in the draft tile, node `row` is seen by the columns whose node has it
+      // on its root path (padding columns see the root only).
+      uint32_t vis[NG];
 #pragma unroll
-      for (int q = 0; q < NG * 32; ++q) {
-        float x = -INFINITY;
-        if (q < NQ) {
-          bool vis = row < valid;
-          if (draft_tile) {
-            const int node = sm->colnode[q];
-            vis = node >= 0 ? (row < n_nodes && ((sm->anc[node] >> row) & 1ull)) : row == 0;
+      for (int gq = 0; gq < NG; ++gq) {
+        const int ncol = min(32, NQ - gq * 32);
+        uint32_t m32 = ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u);
+        if (draft_tile) {
+          uint32_t bits = 0;
+          for (int e = 0; e < ncol; ++e) {
+            const int node = sm->colnode[gq * 32 + e];
+            const bool v = node >= 0 ? (row < n_nodes && ((sm->anc[node] >> row) & 1ull) != 0) : row == 0;
+            bits |= (v ? 1u : 0u) << e;
           }
-          if (vis) x = sv[q] * kScaleLog2;
-          over |= x - sm->m[q] > kThresh;
+          m32 = bits;
+        } else if (row >= valid) {
+          m32 = 0u;
         }
-        sv[q] = x;
+        vis[gq] = m32;
       }
+      // Scores of 32 columns of this thread's token row, base 2, masked to -inf.
+      auto load_scores = [&](int g32, float (&v)[32]) {
+        const uint32_t vm = vis_of(vis, g32);
+        float a[16], cc[16];
+        tmem_ld16(s_addr + g32 * 32, a);
+        const bool second = g32 * 32 + 16 < NQ;
+        if (second) tmem_ld16(s_addr + g32 * 32 + 16, cc);
+        tmem_wait_ld();
+        if (!second) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) cc[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float raw = e < 16 ? a[e] : cc[e - 16];
+          v[e] = ((vm >> e) & 1u) ? raw * kScaleLog2 : -INFINITY;
+        }
+      };
+
+      // Pass 1: does any score exceed its column's running maximum by more than 2^8?
+      float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int g32 = 0; g32 < NG; ++g32) {
+        float v[32], mm[32];
+        load_scores(g32, v);
+        load_cols(sm->m, g32 * 32, mm);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v[e] - mm[e]);
+      }
+      const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
       if (lane == 0) sm->flag[i & 1][sw] = 0;
       __syncwarp();
-      if (__any_sync(0xffffffffu, over) && lane == 0) sm->flag[i & 1][sw] = 1;
+      if (__any_sync(0xffffffffu, dmax > kThresh) && lane == 0) sm->flag[i & 1][sw] = 1;
       if (!group_sync()) break;
       const bool slow = (sm->flag[i & 1][0] | sm->flag[i & 1][1] | sm->flag[i & 1][2] | sm->flag[i & 1][3]) != 0;
       bool pv_waited = false;
       if (slow) {
         // exact column maxima of this tile, new running maxima and rescale factors
-#pragma unroll
-        for (int gq = 0; gq < NG; ++gq) {
+#pragma unroll 1
+        for (int g32 = 0; g32 < NG; ++g32) {
           float v[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = sv[gq * 32 + e];
-          const float mx = transpose_reduce32<true>(v, lane);
-          if (gq * 32 + lane < NQ) sm->red[sw][gq * 32 + lane] = mx;
+          load_scores(g32, v);
+          const float mx = transpose_max32(v, lane);
+          sm->red[sw][g32 * 32 + lane] = mx;
         }
         if (!group_sync()) break;
         for (int q = sw * 32 + lane; q < NQ; q += 128) {
@@ -478,59 +595,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           sm->m[q] = mn;
         }
         if (!group_sync()) break;
-#pragma unroll
-        for (int gq = 0; gq < NG; ++gq)
-          if (gq * 32 + lane < NQ) lcol[gq] *= sm->alpha[gq * 32 + lane];
         if (i > 0) {
-          // O^T holds PV of earlier tiles: wait for the last one, then rescale its columns
+          // O^T and l hold earlier tiles: wait for the last PV, then rescale their columns
           if (!mbar_wait(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
           pv_waited = true;
           tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 3 * NQ / 16; ++c16) {   // O^T low, O^T high, l
+            float v[16];
+            const int col = c16 % (NQ / 16) * 16;
+            const uint32_t a = tmem + lane_addr + kColO + c16 * 16;
+            tmem_ld16(a, v);
+            const float4* al = reinterpret_cast<const float4*>(sm->alpha + col);
+            float f[16];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int c16 = 0; c16 < NQ / 16; ++c16) {
-              float v[16];
-              const uint32_t a = tmem + lane_addr + 2 * NQ + h * NQ + c16 * 16;
-              tmem_ld16(a, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) v[e] *= sm->alpha[c16 * 16 + e];
-              tmem_st16(a, v);
+            for (int k = 0; k < 4; ++k) {
+              const float4 t = al[k];
+              f[4 * k] = t.x; f[4 * k + 1] = t.y; f[4 * k + 2] = t.z; f[4 * k + 3] = t.w;
             }
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= f[e];
+            tmem_st16(a, v);
           }
           tmem_wait_st();
         }
       }
-      // P = exp2(s - m): column sums, then the bf16 P^T row of this token
-#pragma unroll
-      for (int q = 0; q < NG * 32; ++q) sv[q] = q < NQ ? fast_exp2(sv[q] - sm->m[q]) : 0.f;
-#pragma unroll
-      for (int gq = 0; gq < NG; ++gq) {
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = sv[gq * 32 + e];
-        lcol[gq] += transpose_reduce32<false>(v, lane);
-      }
+      // Pass 2: P = exp2(s - m) as the bf16 P^T row of this token.
       if (i > 0 && !pv_waited) {
         if (!mbar_wait(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
       }
+#pragma unroll 1
+      for (int g32 = 0; g32 < NG; ++g32) {
+        float v[32], mm[32];
+        load_scores(g32, v);
+        load_cols(sm->m, g32 * 32, mm);
 #pragma unroll
-      for (int ch = 0; ch < NQ / 8; ++ch) {
-        uint4 v;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-        v.x = *reinterpret_cast<uint32_t*>(&h0);
-        v.y = *reinterpret_cast<uint32_t*>(&h1);
-        v.z = *reinterpret_cast<uint32_t*>(&h2);
-        v.w = *reinterpret_cast<uint32_t*>(&h3);
-        // MN-major P^T: atom ch/8 (64 columns), token row `row`, 16-byte chunk ch%8
-        *reinterpret_cast<uint4*>(sP + (ch >> 3) * kRegionB + sw_off(row, ch & 7)) = v;
+        for (int k = 0; k < 4; ++k) {
+          const int ch = g32 * 4 + k;      // 16-byte chunk (8 columns) of the P^T row
+          if (ch * 8 < NQ) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(fast_exp2(v[k * 8 + 2 * e] - mm[k * 8 + 2 * e]),
+                                                       fast_exp2(v[k * 8 + 2 * e + 1] - mm[k * 8 + 2 * e + 1]));
+              w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            // MN-major P^T: atom ch/8 (64 columns), token row `row`, 16-byte chunk ch%8
+            *reinterpret_cast<uint4*>(sP + (ch >> 3) * kAtomB + p_off(row, ch & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
-      fence_async_smem();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
+      fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL));
     }
@@ -538,45 +657,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // ------------------------------------------------------------ epilogue
     // (every wait is bounded, so warps that disagree after an abort cannot hang)
     if (!*(volatile int*)&sm->abort) {
-#pragma unroll
-      for (int gq = 0; gq < NG; ++gq)
-        if (gq * 32 + lane < NQ) sm->red[sw][gq * 32 + lane] = lcol[gq];
-      bool done = group_sync();
-      for (int q = sw * 32 + lane; q < NQ; q += 128)
-        sm->alpha[q] = sm->red[0][q] + sm->red[1][q] + sm->red[2][q] + sm->red[3][q];  // column sums
-      done = group_sync() && done;
-      done = done && mbar_wait(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status);
+      bool done = mbar_wait(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status);
       tc_fence_after();
+      if (done && sw == 0) {
+        // every lane of l holds the same column sums: warp 0 copies its lane's to shared memory
+#pragma unroll 1
+        for (int c16 = 0; c16 < NQ / 16; ++c16) {
+          float v[16];
+          tmem_ld16(tmem + lane_addr + kColL + c16 * 16, v);
+          tmem_wait_ld();
+          if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sm->alpha[c16 * 16 + e] = v[e];
+          }
+        }
+      }
+      done = group_sync() && done;
+      // per column: 1/l and the output row (node row * 24 + head), or -1 past `rows`
+      for (int q = sw * 32 + lane; q < NQ; q += 128) {
+        sm->red[0][q] = 1.f / sm->alpha[q];
+        sm->colnode[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
+      }
+      done = group_sync() && done;
       if (done) {
         const bool direct = nsplit == 1;
+        const size_t part0 = (size_t)s * bd.total_nodes * kHq;
+#pragma unroll 1
+        for (int c16 = 0; c16 < 2 * NQ / 16; ++c16) {
+          const int h = c16 / (NQ / 16);
+          const int col = c16 % (NQ / 16) * 16;
+          float v[16];
+          tmem_ld16(tmem + lane_addr + kColO + c16 * 16, v);
+          float inv[16];
+          int orow[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+          for (int k = 0; k < 4; ++k) {
+            const float4 a = reinterpret_cast<const float4*>(sm->red[0] + col)[k];
+            const int4 o = reinterpret_cast<const int4*>(sm->colnode + col)[k];
+            inv[4 * k] = a.x; inv[4 * k + 1] = a.y; inv[4 * k + 2] = a.z; inv[4 * k + 3] = a.w;
+            orow[4 * k] = o.x; orow[4 * k + 1] = o.y; orow[4 * k + 2] = o.z; orow[4 * k + 3] = o.w;
+          }
+          tmem_wait_ld();
+          const int d = h * 128 + row;
 #pragma unroll
-          for (int c16 = 0; c16 < NQ / 16; ++c16) {
-            float v[16];
-            tmem_ld16(tmem + lane_addr + 2 * NQ + h * NQ + c16 * 16, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int q = c16 * 16 + e;
-              if (q >= rows) continue;
-              const int r = q0 + q / hpc;
-              const int head = head0 + q % hpc;
-              const float o = v[e] / sm->alpha[q];
-              const int d = h * 128 + row;
-              if (direct) p.out[((size_t)r * kHq + head) * kDim + d] = __float2bfloat16_rn(o);
-              else p.o_part[(((size_t)s * bd.total_nodes + r) * kHq + head) * kDim + d] = o;
-            }
+          for (int e = 0; e < 16; ++e) {
+            if (orow[e] < 0) continue;
+            const float o = v[e] * inv[e];
+            if (direct) p.out[(size_t)orow[e] * kDim + d] = __float2bfloat16_rn(o);
+            else p.o_part[(part0 + orow[e]) * kDim + d] = o;
           }
         }
         for (int q = sw * 32 + lane; q < rows; q += 128) {
-          const int r = q0 + q / hpc;
-          const int head = head0 + q % hpc;
           const float lse2 = sm->m[q] + fast_log2(sm->alpha[q]);
           if (direct) {
-            if (p.lse != nullptr) p.lse[(size_t)r * kHq + head] = lse2 * kLn2;
+            if (p.lse != nullptr) p.lse[sm->colnode[q]] = lse2 * kLn2;
           } else {
-            p.lse_part[((size_t)s * bd.total_nodes + r) * kHq + head] = lse2;
+            p.lse_part[part0 + sm->colnode[q]] = lse2;
           }
         }
       }
@@ -584,10 +720,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
 
   tc_fence_before();
+  }  // compute warps
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm->tmem));
   }
 }
 
@@ -606,7 +743,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [pool pages * 4 heads * 16 slots] rows of 256 bf16; boxes of 16 rows x 64 dims, 128-byte swizzle.
+// The cache as [pool pages * 4 KV heads * 16 slots] rows of 256 bf16; a box
+// of 16 rows x 64 dims (one page of one head, one 64-dim block) lands as 16
+// rows x 128 B with the 128-byte swizzle.
 bool cache_map(CUtensorMap* map, const void* cache, int pool_pages) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -634,7 +773,7 @@ cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnPa
 
 size_t tc_smem_bytes(int nq) {
   const int natom = (nq + 63) / 64;
-  return 1024 + (size_t)nq * 512 + 2 * (size_t)kTileB + (size_t)natom * kRegionB + sizeof(Small);
+  return (size_t)nq * 512 + 2 * (size_t)kTileB + (size_t)natom * kAtomB + kOnesB + sizeof(Small);
 }
 
 TcPlan tc_plan(int max_nodes) {
@@ -664,7 +803,6 @@ cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_
     case 64: e = launch_nq<64>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
     case 80: e = launch_nq<80>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
     case 96: e = launch_nq<96>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
-    case 112: e = launch_nq<112>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess || p.num_splits == 1) return e;

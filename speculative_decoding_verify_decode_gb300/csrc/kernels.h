@@ -5,13 +5,8 @@
 
 namespace sdv {
 
-// Verify attention on mma.sync tiles: split kernel (+ merge when num_splits > 1).
-int attn_mma_tile();
-int attn_mma_ctas_per_split(const BatchDesc& bd);
-cudaError_t launch_attn_mma(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
-
 // Verify attention on tcgen05 tiles with TMA-staged pages (+ merge when num_splits > 1).
-constexpr int kTcMaxNQ = 112;   // query columns per CTA (heads-per-CTA x nodes, padded to 16)
+constexpr int kTcMaxNQ = 96;    // query columns per CTA (heads-per-CTA x nodes, padded to 16)
 struct TcPlan {
   int hpc;      // query heads of a KV group handled by one CTA: 6, 3, 2 or 1
   int hparts;   // CTAs per (split, KV head): ceil(6 / hpc)

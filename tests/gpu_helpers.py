@@ -27,6 +27,9 @@ def f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float32).numpy()
 
 
+LSE_TOL = 4e-3
+
+
 def attn_bound(ref: np.ndarray) -> float:
     """The contract: max |err| <= 2e-2 * max |ref| + 1e-3."""
     return 2e-2 * float(np.abs(ref).max()) + 1e-3
@@ -46,8 +49,10 @@ def check_attention(out: torch.Tensor, ref: np.ndarray, lse: torch.Tensor | None
     assert err <= tight_bound(ref), (err, tight_bound(ref))
     out = {"max_err": err, "max_ref": float(np.abs(ref).max())}
     if lse is not None:
+        # the kernel normalises by the sum of the bf16-rounded weights it also
+        # multiplies V with, so the log-sum-exp carries bf16 rounding: |d lse| <= ln(1 + 2^-8)
         lerr = float(np.abs(f64(lse) - ref_lse).max())
-        assert lerr <= 1e-4 * float(np.abs(ref_lse).max()) + 2e-4, lerr
+        assert lerr <= LSE_TOL, lerr
         out["lse_err"] = lerr
     return out
 

@@ -73,6 +73,15 @@ def test_null_pointers_and_workspace(lib):
     assert _attn(lib, big, ws=FAKE, ws_bytes=need - 1) == native.SD_ERR_WORKSPACE
 
 
+def test_misaligned_tensors_rejected(lib):
+    assert _attn(lib, _shape(), q=FAKE + 8) == native.SD_ERR_INVALID_ARG
+    s = _shape()
+    arr = (ctypes.c_void_p * 1)(FAKE + 2)
+    ok = (ctypes.c_void_p * 1)(FAKE)
+    assert lib.sd_kv_commit(s.ref, 1, arr, ok, ok, ok, FAKE, FAKE, None, FAKE, FAKE, 8, None, None) \
+        == native.SD_ERR_INVALID_ARG
+
+
 def test_workspace_grows_with_context_and_nodes(lib):
     a = lib.sd_verify_attn_workspace_size(_shape((0, 9), max_pages=257, pool=257).ref)
     b = lib.sd_verify_attn_workspace_size(_shape((0, 23), max_pages=8194, pool=8194).ref)
