@@ -135,6 +135,36 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
                          void* out, float* lse, void* workspace, size_t ws_bytes,
                          int* dev_status, void* stream);
 
+/*
+ * sd_verify_attn_noalloc — sd_verify_attn for callers that cannot allocate
+ * device memory (the pages have no counterpart: this is a library entry point,
+ * not part of the method).
+ *
+ * Some callers cannot make or hold a device allocation where they call us:
+ * a plugin running inside another runtime whose device memory belongs to that
+ * runtime's pool, or a decode loop on a path where allocating (and the
+ * synchronisation it may cause) is not allowed.  This entry point takes the
+ * same inputs and outputs as sd_verify_attn but no workspace: the split
+ * partials go to a scratch array of SD_NOALLOC_SCRATCH_BYTES that the library
+ * keeps in device memory (every GPU that loads the library holds it until the
+ * process exits).  It allocates nothing and calls no allocating routine.
+ *
+ *  - The first call on each device looks up the array's address on that
+ *    device (with it current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero).  Calls that may overlap on the GPU
+ *    — on unordered streams or from several threads — race on it.
+ *  - A shape whose scratch need (sd_verify_attn_workspace_size) exceeds
+ *    SD_NOALLOC_SCRATCH_BYTES is rejected with SD_ERR_WORKSPACE before any
+ *    launch.  Other arguments and errors are as for sd_verify_attn.
+ */
+#define SD_NOALLOC_SCRATCH_BYTES (16u << 20)
+sd_status sd_verify_attn_noalloc(const sd_shape* shape, const void* q, const void* k_cache,
+                                 const void* v_cache, const void* k_new, const void* v_new,
+                                 const int* page_table, const int* ctx_lens, const int* parents,
+                                 void* out, float* lse, int* dev_status, void* stream);
+
 /* Bytes of workspace sd_accept needs (0 on bad arguments). */
 size_t sd_accept_workspace_size(int batch, const int* q_indptr_h, int vocab);
 

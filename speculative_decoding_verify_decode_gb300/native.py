@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
     lib.sd_verify_attn_workspace_size.argtypes = [shp]
     lib.sd_verify_attn.restype = ctypes.c_int
     lib.sd_verify_attn.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, fp, vp, sz, vp, vp]
+    lib.sd_verify_attn_noalloc.restype = ctypes.c_int
+    lib.sd_verify_attn_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, fp, vp, vp]
     lib.sd_accept_workspace_size.restype = sz
     lib.sd_accept_workspace_size.argtypes = [ctypes.c_int, ip, ctypes.c_int]
     lib.sd_accept.restype = ctypes.c_int
@@ -132,6 +134,18 @@ def sd_verify_attn(shape: Shape, q, k_cache, v_cache, k_new, v_new, page_table, 
                                  _ptr(page_table), _ptr(ctx_lens), _ptr(parents), _ptr(out), _ptr(lse),
                                  _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
            "sd_verify_attn")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def sd_verify_attn_noalloc(shape: Shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, out,
+                           lse=None, dev_status=None, stream=None) -> None:
+    """sd_verify_attn with the library's fixed scratch array instead of a caller workspace."""
+    _check(load().sd_verify_attn_noalloc(shape.ref, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
+                                         _ptr(v_new), _ptr(page_table), _ptr(ctx_lens), _ptr(parents), _ptr(out),
+                                         _ptr(lse), _ptr(dev_status), _stream(stream)),
+           "sd_verify_attn_noalloc")
 
 
 def sd_accept_workspace_size(q_indptr, vocab: int) -> int:
