@@ -162,7 +162,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     native.load()
-    w = synth.make_workload(args.config, device=dev)
+    w = synth.make_workload(args.config, device=dev, layers=args.layers or None)
     d = device_inputs(w, dev)
     step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev,
                       num_splits=args.splits)
@@ -340,6 +340,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers of the workload to build (0 = its own count; fewer only for profiler captures)")
     ap.add_argument("--splits", type=int, default=0, help="split-KV chunks per (sequence, KV head); 0 = auto")
     args = ap.parse_args()
     world, rank, local = dist_setup()

@@ -51,11 +51,11 @@ int device_sm_count() {
 }
 
 struct SplitPlan {
-  int chunk;     // context tokens per split
-  int nsplit;    // splits in the grid
+  int chunk;     // context tokens per context split
+  int nsplit;    // splits in the grid: the draft split + the context splits
 };
 
-// Context tokens per split.  Every split CTA (one per SM) pays a fixed
+// Context tokens per context split.  Every split CTA (one per SM) pays a fixed
 // set-up and epilogue, so a single sequence gets one wave of CTAs, each with
 // an equal share of the 128-token tiles; a batch, whose context lengths are
 // not known on the host, is cut for two waves of the worst case (every
@@ -70,14 +70,14 @@ SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
   } else {
     const long long streams = (long long)bd.batch * kHkv * tc_plan(bd.max_nodes).hparts;
     const long long waves = bd.batch > 1 ? 2 : 1;
-    const long long slots = waves * device_sm_count();
+    long long slots = waves * device_sm_count() - streams;    // the draft CTAs take one slot per stream
+    if (slots < streams) slots = streams;
     const long long per_cta = (streams * max_tiles + slots - 1) / slots;
     chunk = (per_cta < 1 ? 1 : per_cta) * tile;
   }
   chunk = (chunk + tile - 1) / tile * tile;
   if (chunk < tile) chunk = tile;
-  long long n = (max_ctx + chunk - 1) / chunk;
-  if (n < 1) n = 1;
+  const long long n = 1 + (max_ctx + chunk - 1) / chunk;   // the draft split + the context chunks
   return SplitPlan{(int)chunk, (int)n};
 }
 

@@ -66,15 +66,18 @@ struct Small {
   float m[kCols];
   float alpha[kCols];
   float red[4][kCols];
-  int colnode[kCols];
+  int outrow[kCols];    // output row (node row * 24 + head) of each query column (-1: padding)
   uint64_t bar[NUM_BARS];
-  uint64_t anc[kMaxNodes];
+  unsigned long long anc[kMaxNodes];    // bit r of anc[n]: draft node r is node n or one of its ancestors
+  unsigned long long desc[kMaxNodes];   // bit n of desc[r]: the same relation, transposed
+  int par[kMaxNodes];
   int flag[2][4];
   uint32_t tmem;
   int abort;
 };
 static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &&
-                  offsetof(Small, red) % 16 == 0 && offsetof(Small, colnode) % 16 == 0,
+                  offsetof(Small, red) % 16 == 0 &&
+                  offsetof(Small, outrow) % 16 == 0,
               "per-column arrays must be 16-byte aligned");
 static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 
@@ -128,6 +131,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Small* 
   }
   return true;
 }
+// Bounded spin on a phase (no suspension): the softmax warps have nothing
+// else to do while they wait, and a spin sees the phase flip soonest.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, Small* sm, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
+      sm->abort = 1;
+      report(status, SD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -135,6 +151,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Bulk copy shared -> global (async proxy); addresses and size multiples of 16 bytes.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+// Close this thread's bulk group and wait until its copies have completed.
+__device__ __forceinline__ void bulk_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------ tcgen05
@@ -226,6 +253,38 @@ __device__ __forceinline__ void stage_rows(uint8_t* base, int rows, int r0, int 
   }
 }
 
+// Copy `nrows` rows of 256 bf16 into group-major tiles: row i comes from
+// src_of(i) (zeros when null) and lands at the shared-memory byte offset
+// dst_of(i, chunk).  `nthreads` threads starting at `t` share the 16-byte
+// chunks, up to 16 loads in flight per thread; the last round re-copies the
+// final chunk instead of branching, so the unrolled copies stay independent.
+template <typename SrcFn, typename DstFn>
+__device__ __forceinline__ void stage_rows_fast(int nrows, SrcFn src_of, DstFn dst_of, int t, int nthreads) {
+  constexpr int U = 16;
+  const int tasks = nrows * 32;
+  for (int t0 = t; t0 - t < tasks; t0 += nthreads * U) {
+    uint4 v[U];
+    uint8_t* dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int task = min(t0 + u * nthreads, tasks - 1);
+      const __nv_bfloat16* src = src_of(task >> 5);
+      v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + (task & 31)) : make_uint4(0, 0, 0, 0);
+      dst[u] = dst_of(task >> 5, task & 31);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dst[u]) = v[u];
+  }
+}
+
+// Bits [start, start + len) of a 32-bit word (clipped to the word).
+__device__ __forceinline__ uint32_t bit_range(int start, int len) {
+  const int a = max(start, 0), e = min(start + len, 32);
+  if (e <= a) return 0u;
+  const uint32_t upto = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+  return upto & ~((1u << a) - 1u);
+}
+
 // Element g of a small per-thread array, by a select chain rather than a
 // dynamically indexed (local-memory) access.
 template <int N>
@@ -282,6 +341,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_nodes = bd.q_indptr[b + 1] - q0;
   const int rows = hpc * n_nodes;
   if (c * hpc >= kGroup) return;
+  // Launched as a programmatic dependent: wait for the previous kernel in the
+  // stream before touching global memory, then let the merge kernel's blocks
+  // be scheduled (they wait for this grid to finish before reading).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Split 0 attends to the draft block alone; split s >= 1 to context tokens
+  // [(s - 1) * chunk, s * chunk).  The producers fetch their first tile's page
+  // ids beside the context length (any entry of the table row is in bounds).
+  const bool has_draft = (s == 0);
+  int page0 = -1;
+  if ((warp == kWarpK || warp == kWarpV) && lane < 8 && !has_draft) {
+    const long long idx = (((long long)(s - 1) * p.chunk) >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
   int L = p.ctx_lens[b];
   if (L < 0 || L > p.max_pages * kPage) {
     if (s == 0 && c == 0 && g == 0 && tid == 0) report(p.dev_status, SD_DEV_BAD_CTX);
@@ -289,11 +362,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   const int nsplit = active_splits(L, p.chunk);
   if (s >= nsplit) return;
-  const int ctx_begin = s * p.chunk;
-  const int ctx_end = min(L, ctx_begin + p.chunk);
-  const bool has_draft = (s == 0);
-  const int n_ctx_tiles = ctx_end > ctx_begin ? (ctx_end - ctx_begin + kT - 1) / kT : 0;
-  const int n_tiles = n_ctx_tiles + (has_draft ? 1 : 0);
+  const int ctx_begin = has_draft ? 0 : (s - 1) * p.chunk;
+  const int ctx_end = has_draft ? 0 : min(L, ctx_begin + p.chunk);
+  const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
   const int head0 = g * kGroup + c * hpc;
   if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
     if (threadIdx.x == 0) report(p.dev_status, SD_DEV_TIMEOUT);
@@ -311,28 +382,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   for (int q = tid; q < kCols; q += kThreads) {
     sm->m[q] = q < NQ ? -INFINITY : 0.f;
-    sm->colnode[q] = q < rows ? q / hpc : -1;
+    sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
   }
   for (int i = tid; i < kOnesB / 16; i += kThreads)   // bf16 1.0 = 0x3F80
     reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  if (has_draft && tid < n_nodes) {
-    // ancestor bitmask of node tid (bit i: i is tid or an ancestor of tid)
-    uint64_t mask = 1ull << tid;
-    bool ok = true;
-    if (tid == 0) {
-      ok = p.parents[q0] == -1;
-    } else {
-      int u = tid;
-      while (u > 0) {
-        const int pu = p.parents[q0 + u];
-        if (pu < 0 || pu >= u) { ok = false; break; }
-        mask |= 1ull << pu;
-        u = pu;
-      }
-    }
-    if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); mask = 1ull << tid; }
-    sm->anc[tid] = mask;
-  }
+  if (has_draft && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];   // one load each; the walk below is in shared memory
   __syncthreads();  // mbarriers and per-column arrays ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -344,20 +398,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const uint32_t full = bar(is_k ? K_FULL : V_FULL), empty = bar(is_k ? K_EMPTY : V_EMPTY);
-    const int first = has_draft ? 1 : 0;
-    const uint32_t init_full = has_draft ? 1u : 0u;
-    for (int i = first; i < n_tiles; ++i) {
-      const int t0 = ctx_begin + (i - first) * kT;
+    const int n_ctx = has_draft ? 0 : n_tiles;   // the draft CTA stages its block without TMA
+    for (int i = 0; i < n_ctx; ++i) {
+      const int t0 = ctx_begin + i * kT;
       const int valid = min(kT, ctx_end - t0);
       int page = -1;
       if (lane < 8 && lane * kPage < valid) {
-        page = p.page_table[(size_t)b * p.max_pages + ((t0 >> 4) + lane)];
+        page = i == 0 ? page0 : p.page_table[(size_t)b * p.max_pages + ((t0 >> 4) + lane)];
         if (page < 0 || page >= p.num_pool_pages) { report(p.dev_status, SD_DEV_BAD_PAGE); page = -1; }
       }
       // a page goes by TMA when it is in range and all 16 of its tokens are valid
       const bool page_full = page >= 0 && (lane + 1) * kPage <= valid;
       const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page_full);
-      const uint32_t parity = (uint32_t)((i - first) & 1) ^ init_full ^ 1u;
+      const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
@@ -389,17 +442,54 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // (and split 0's draft block, tile 0) and allocate tensor memory.
   {
     const int ct = tid - 32, nct = 5 * 32;
-    // Q^T (K-major): column q = node * hpc + head-in-part; zero columns past `rows`.
-    stage_rows(sQ, NQ, 0, NQ, [&](int q) -> const __nv_bfloat16* {
-      return q < rows ? p.q + ((size_t)(q0 + q / hpc) * kHq + head0 + q % hpc) * kDim : nullptr;
+    // One pass of row copies with every load in flight at once:
+    //   Q^T (K-major): column q = node * hpc + head-in-part (the hpc heads of
+    //   a node are adjacent rows of q), zero past `rows`;
+    //   draft CTA only: the draft block as the K and V tile, node t = token
+    //   row t.  K rows past the block are left stale (their scores are
+    //   masked); V rows past it are zeroed below (P^T is 0 there, and 0 times
+    //   stale shared memory could be NaN).
+    const int k_rows = has_draft ? n_nodes : 0;
+    const float inv_hpc = 1.0f / (float)hpc;
+    const __nv_bfloat16* q_base = p.q + ((size_t)q0 * kHq + head0) * kDim;
+    stage_rows_fast(NQ + 2 * k_rows, [&](int vr) -> const __nv_bfloat16* {
+      if (vr < NQ) {
+        const int node = __float2int_rz(((float)vr + 0.5f) * inv_hpc);   // vr / hpc, exact for vr < 2^20
+        return vr < rows ? q_base + (size_t)(node * kHq + (vr - node * hpc)) * kDim : nullptr;
+      }
+      vr -= NQ;
+      const __nv_bfloat16* base = vr < k_rows ? p.k_new : p.v_new;
+      vr = vr < k_rows ? vr : vr - k_rows;
+      return base + ((size_t)(q0 + vr) * kHkv + g) * kDim;
+    }, [&](int vr, int chunk) -> uint8_t* {
+      if (vr < NQ) return sQ + tile_off(NQ, vr, chunk);
+      vr -= NQ;
+      return (vr < k_rows ? sK + tile_off(kT, vr, chunk) : sV + tile_off(kT, vr - k_rows, chunk));
     }, ct, nct);
-    if (has_draft) {  // the draft block is tile 0 of split 0: node t is token row t
-      stage_rows(sK, kT, 0, kT, [&](int t) -> const __nv_bfloat16* {
-        return t < n_nodes ? p.k_new + ((size_t)(q0 + t) * kHkv + g) * kDim : nullptr;
-      }, ct, nct);
-      stage_rows(sV, kT, 0, kT, [&](int t) -> const __nv_bfloat16* {
-        return t < n_nodes ? p.v_new + ((size_t)(q0 + t) * kHkv + g) * kDim : nullptr;
-      }, ct, nct);
+    if (has_draft) {
+      for (int i = ct; i < (kT - n_nodes) * 32; i += nct)
+        *reinterpret_cast<uint4*>(sV + tile_off(kT, n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
+      // Ancestor set of node ct by walking its root path, then (after the
+      // compute warps' barrier) the descendant set of node ct as the
+      // transpose: no shared-memory atomics.
+      if (ct < n_nodes) {
+        unsigned long long a = 1ull << ct;
+        bool ok = ct == 0 ? sm->par[0] == -1 : true;
+        for (int u = ct; ok && u > 0;) {
+          const int pu = sm->par[u];
+          ok = pu >= 0 && pu < u;
+          if (ok) a |= 1ull << pu;
+          u = pu;
+        }
+        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << ct; }
+        sm->anc[ct] = a;
+      }
+      asm volatile("bar.sync 2, 160;" ::: "memory");   // the five compute warps of the draft CTA
+      if (ct < n_nodes) {
+        unsigned long long d = 0ull;
+        for (int n = ct; n < n_nodes; ++n) d |= ((sm->anc[n] >> ct) & 1ull) << n;
+        sm->desc[ct] = d;
+      }
     }
     if (warp == kWarpMma) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
@@ -501,7 +591,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     auto group_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(GROUP));
-      return mbar_wait(bar(GROUP), (uint32_t)(gphase++ & 1), sm, p.dev_status);
+      return mbar_spin(bar(GROUP), (uint32_t)(gphase++ & 1), sm, p.dev_status);
     };
     auto load_cols = [&](const float* arr, int col, float (&w)[32]) {
       const float4* src = reinterpret_cast<const float4*>(arr + col);
@@ -513,33 +603,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     };
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
-      if (!mbar_wait(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
+      if (!mbar_spin(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + kColS0 + sb * NQ;
-      const bool draft_tile = has_draft && i == 0;
-      const int t0 = ctx_begin + (i - (has_draft ? 1 : 0)) * kT;
+      const bool draft_tile = has_draft;
+      const int t0 = ctx_begin + i * kT;
       const int valid = draft_tile ? n_nodes : min(kT, ctx_end - t0);
       // Visibility of this thread's token row, one bit per column of each
       // 32-column group: context rows before `valid` see every query column;
-      // in the draft tile, node `row` is seen by the columns whose node has it
-      // on its root path (padding columns see the root only).
+      // in the draft tile, node `row` is seen by the columns of its
+      // descendants (itself included; padding columns see the root only).
       uint32_t vis[NG];
 #pragma unroll
       for (int gq = 0; gq < NG; ++gq) {
         const int ncol = min(32, NQ - gq * 32);
-        uint32_t m32 = ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u);
-        if (draft_tile) {
-          uint32_t bits = 0;
-          for (int e = 0; e < ncol; ++e) {
-            const int node = sm->colnode[gq * 32 + e];
-            const bool v = node >= 0 ? (row < n_nodes && ((sm->anc[node] >> row) & 1ull) != 0) : row == 0;
-            bits |= (v ? 1u : 0u) << e;
-          }
-          m32 = bits;
-        } else if (row >= valid) {
-          m32 = 0u;
+        vis[gq] = (!draft_tile && row < valid) ? (ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u)) : 0u;
+      }
+      if (draft_tile) {
+        unsigned long long d = row < n_nodes ? sm->desc[row] : 0ull;
+        while (d != 0ull) {
+          const int n = __ffsll((long long)d) - 1;
+          d &= d - 1ull;
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(n * hpc - gq * 32, hpc);
         }
-        vis[gq] = m32;
+        if (row == 0) {
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(rows - gq * 32, NQ - rows);
+        }
       }
       // Scores of 32 columns of this thread's token row, base 2, masked to -inf.
       auto load_scores = [&](int g32, float (&v)[32]) {
@@ -597,7 +688,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!group_sync()) break;
         if (i > 0) {
           // O^T and l hold earlier tiles: wait for the last PV, then rescale their columns
-          if (!mbar_wait(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+          if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
           pv_waited = true;
           tc_fence_after();
 #pragma unroll 1
@@ -623,7 +714,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
       // Pass 2: P = exp2(s - m) as the bf16 P^T row of this token.
       if (i > 0 && !pv_waited) {
-        if (!mbar_wait(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+        if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
       }
 #pragma unroll 1
       for (int g32 = 0; g32 < NG; ++g32) {
@@ -655,66 +746,75 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
 
     // ------------------------------------------------------------ epilogue
-    // (every wait is bounded, so warps that disagree after an abort cannot hang)
-    if (!*(volatile int*)&sm->abort) {
-      bool done = mbar_wait(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status);
+    // Each thread owns dims `row` and 128 + `row` of every query column.  The
+    // column sums l sit in every tensor-memory lane, so each thread reads the
+    // ones it needs beside its O^T values.  The normalised rows are staged in
+    // the idle K/V tiles (256 values per query column, columns of one node
+    // adjacent, as are their output rows) and leave with one bulk copy per
+    // node: far fewer memory requests than per-thread stores.
+    if (!*(volatile int*)&sm->abort && mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
       tc_fence_after();
-      if (done && sw == 0) {
-        // every lane of l holds the same column sums: warp 0 copies its lane's to shared memory
+      const bool direct = nsplit == 1;
+      const size_t part0 = (size_t)s * bd.total_nodes * kHq;
+      const uint32_t t_row = tmem + lane_addr;
+      float* stage_f = reinterpret_cast<float*>(sK);
+      __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(sK);
 #pragma unroll 1
-        for (int c16 = 0; c16 < NQ / 16; ++c16) {
-          float v[16];
-          tmem_ld16(tmem + lane_addr + kColL + c16 * 16, v);
-          tmem_wait_ld();
-          if (lane == 0) {
+      for (int col = 0; col < NQ; col += 16) {
+        float lo[16], hi[16], l[16];
+        tmem_ld16(t_row + kColO + col, lo);
+        tmem_ld16(t_row + kColO + NQ + col, hi);
+        tmem_ld16(t_row + kColL + col, l);
+        tmem_wait_ld();
+        // every column is written (padding columns too: the staging area holds
+        // NQ rows), so the 16 columns stay independent of each other
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sm->alpha[c16 * 16 + e] = v[e];
-          }
-        }
-      }
-      done = group_sync() && done;
-      // per column: 1/l and the output row (node row * 24 + head), or -1 past `rows`
-      for (int q = sw * 32 + lane; q < NQ; q += 128) {
-        sm->red[0][q] = 1.f / sm->alpha[q];
-        sm->colnode[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
-      }
-      done = group_sync() && done;
-      if (done) {
-        const bool direct = nsplit == 1;
-        const size_t part0 = (size_t)s * bd.total_nodes * kHq;
-#pragma unroll 1
-        for (int c16 = 0; c16 < 2 * NQ / 16; ++c16) {
-          const int h = c16 / (NQ / 16);
-          const int col = c16 % (NQ / 16) * 16;
-          float v[16];
-          tmem_ld16(tmem + lane_addr + kColO + c16 * 16, v);
-          float inv[16];
-          int orow[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float4 a = reinterpret_cast<const float4*>(sm->red[0] + col)[k];
-            const int4 o = reinterpret_cast<const int4*>(sm->colnode + col)[k];
-            inv[4 * k] = a.x; inv[4 * k + 1] = a.y; inv[4 * k + 2] = a.z; inv[4 * k + 3] = a.w;
-            orow[4 * k] = o.x; orow[4 * k + 1] = o.y; orow[4 * k + 2] = o.z; orow[4 * k + 3] = o.w;
-          }
-          tmem_wait_ld();
-          const int d = h * 128 + row;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            if (orow[e] < 0) continue;
-            const float o = v[e] * inv[e];
-            if (direct) p.out[(size_t)orow[e] * kDim + d] = __float2bfloat16_rn(o);
-            else p.o_part[(part0 + orow[e]) * kDim + d] = o;
-          }
-        }
-        for (int q = sw * 32 + lane; q < rows; q += 128) {
-          const float lse2 = sm->m[q] + fast_log2(sm->alpha[q]);
+        for (int e = 0; e < 16; ++e) {
+          const int q = col + e;
+          const float inv = __fdividef(1.0f, l[e]);
           if (direct) {
-            if (p.lse != nullptr) p.lse[sm->colnode[q]] = lse2 * kLn2;
+            stage_h[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
+            stage_h[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
           } else {
-            p.lse_part[part0 + sm->colnode[q]] = lse2;
+            stage_f[q * kDim + row] = lo[e] * inv;
+            stage_f[q * kDim + 128 + row] = hi[e] * inv;
           }
         }
+      }
+      fence_async_smem();   // the staged rows are read by the bulk copies (async proxy)
+      // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
+      if (sw * 32 < rows) {
+        float l32[32];
+        {
+          float a[16], c2[16];
+          tmem_ld16(t_row + kColL + sw * 32, a);
+          tmem_ld16(t_row + kColL + sw * 32 + 16, c2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { l32[e] = a[e]; l32[e + 16] = c2[e]; }
+        }
+        float lq = l32[0];
+#pragma unroll
+        for (int e = 1; e < 32; ++e) lq = lane == e ? l32[e] : lq;
+        const int q = sw * 32 + lane;
+        if (q < rows) {
+          const float lse2 = sm->m[q] + fast_log2(lq);
+          if (direct) {
+            if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
+          } else {
+            p.lse_part[part0 + sm->outrow[q]] = lse2;
+          }
+        }
+      }
+      if (group_sync() && sw == 0) {
+        const int row_b = direct ? kDim * 2 : kDim * 4;
+        for (int n = lane; n < n_nodes; n += 32) {
+          const size_t orow0 = (size_t)(q0 + n) * kHq + head0;
+          void* dst = direct ? static_cast<void*>(p.out + orow0 * kDim)
+                             : static_cast<void*>(p.o_part + (part0 + orow0) * kDim);
+          bulk_store(dst, smem_u32(sK + n * hpc * row_b), (uint32_t)(hpc * row_b));
+        }
+        bulk_commit_and_wait();
       }
     }
   }
@@ -764,9 +864,17 @@ cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnPa
   const size_t smem = tc_smem_bytes(NQ);
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.num_splits * kHkv * hparts, bd.batch);
-  attn_tc_kernel<NQ><<<grid, kThreads, smem, st>>>(mk, mv, p, bd, hpc, hparts);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits * kHkv * hparts, bd.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ>, mk, mv, p, bd, hpc, hparts);
 }
 
 }  // namespace

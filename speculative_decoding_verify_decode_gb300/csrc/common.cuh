@@ -68,11 +68,11 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
-// Number of active splits of a sequence with context length L (>= 1: the
-// first split also carries the draft block, even when L == 0).
+// Number of active splits of a sequence with context length L: split 0
+// attends to the draft block alone and splits 1.. to consecutive chunks of
+// `chunk` context tokens, so a sequence without context has one split.
 __host__ __device__ __forceinline__ int active_splits(int L, int chunk) {
-  int n = (L + chunk - 1) / chunk;
-  return n < 1 ? 1 : n;
+  return 1 + (L > 0 ? (L + chunk - 1) / chunk : 0);
 }
 
 }  // namespace sdv
