@@ -48,8 +48,9 @@ namespace sdv {
 namespace {
 
 constexpr int kT = 128;                 // tokens per tile
-constexpr int kRegionB = kT * 128;      // one 64-dim block of a K/V tile: 128 rows x 128 B = 16 KB
-constexpr int kTileB = 4 * kRegionB;    // 64 KB
+constexpr int kGroupB = 4096;           // 8 token rows x 4 dim blocks x 128 B
+constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 256 dims
+constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
 constexpr int kOnesB = 1024;            // the all-ones operand: 8 rows x 128 B
 constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
 constexpr int kThreads = 224;
@@ -146,22 +147,13 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, Small* 
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// One page of one KV head (8 KB) into shared memory: the 4-D box of the
+// cache map at outer coordinate w, x = y = z = 0.
+__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int w, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
       : "memory");
-}
-
-// Bulk copy shared -> global (async proxy); addresses and size multiples of 16 bytes.
-__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-// Close this thread's bulk group and wait until its copies have completed.
-__device__ __forceinline__ void bulk_commit_and_wait() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------ tcgen05
@@ -215,10 +207,16 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 
-// Byte offset of 16-byte chunk c (0..31) of row r in a group-major operand
-// tile: group r/8, 64-dim block c/8, row r%8, swizzled chunk (c%8) ^ (r%8).
+// Byte offset of 16-byte chunk c (0..31) of row r in the block-major Q^T
+// tile of `rows` rows: 64-dim block c/8, row r, swizzled chunk (c%8) ^ (r%8).
 __device__ __forceinline__ uint32_t tile_off(int rows, int r, int c) {
   return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// Byte offset of 16-byte chunk c (0..31) of token row r in a group-major
+// K/V tile: 8-row group r/8 (4 KB), 64-dim block c/8 (1 KB), row r%8,
+// swizzled chunk (c%8) ^ (r%8).  A page's 16 rows are 8 contiguous KB.
+__device__ __forceinline__ uint32_t kv_off(int r, int c) {
+  return (uint32_t)((r >> 3) * kGroupB + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 // Byte offset of 16-byte chunk cc (0..7) of token row r in the P^T tile
 // (MN-major: 64-column atoms of 128 rows x 128 B, 128-byte swizzle).
@@ -226,12 +224,12 @@ __device__ __forceinline__ uint32_t p_off(int r, int cc) {
   return (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
 }
 
-// Copy `nrows` rows of 256 bf16 into a group-major tile (row r's source is
-// src_of(r), or zeros when that is null).  `nthreads` threads starting at `t`
-// share the work; each keeps 8 independent 16-byte loads in flight.
+// Copy `nrows` rows of 256 bf16 into rows r0.. of a group-major K/V tile
+// (row r's source is src_of(r), or zeros when that is null).  `nthreads`
+// threads starting at `t` share the work; each keeps 8 independent 16-byte
+// loads in flight.
 template <typename SrcFn>
-__device__ __forceinline__ void stage_rows(uint8_t* base, int rows, int r0, int nrows, SrcFn src_of, int t,
-                                           int nthreads) {
+__device__ __forceinline__ void stage_rows(uint8_t* base, int r0, int nrows, SrcFn src_of, int t, int nthreads) {
   constexpr int U = 8;
   const int tasks = nrows * 32;
   for (int t0 = t; t0 < tasks; t0 += nthreads * U) {
@@ -248,7 +246,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* base, int rows, int r0, int 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int task = t0 + u * nthreads;
-      if (task < tasks) *reinterpret_cast<uint4*>(base + tile_off(rows, r0 + (task >> 5), task & 31)) = v[u];
+      if (task < tasks) *reinterpret_cast<uint4*>(base + kv_off(r0 + (task >> 5), task & 31)) = v[u];
     }
   }
 }
@@ -399,13 +397,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const uint32_t full = bar(is_k ? K_FULL : V_FULL), empty = bar(is_k ? K_EMPTY : V_EMPTY);
     const int n_ctx = has_draft ? 0 : n_tiles;   // the draft CTA stages its block without TMA
+    int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
     for (int i = 0; i < n_ctx; ++i) {
       const int t0 = ctx_begin + i * kT;
       const int valid = min(kT, ctx_end - t0);
-      int page = -1;
-      if (lane < 8 && lane * kPage < valid) {
-        page = i == 0 ? page0 : p.page_table[(size_t)b * p.max_pages + ((t0 >> 4) + lane)];
-        if (page < 0 || page >= p.num_pool_pages) { report(p.dev_status, SD_DEV_BAD_PAGE); page = -1; }
+      int page = (lane < 8 && lane * kPage < valid) ? page_next : -1;
+      if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
+        page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
+      if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
+        report(p.dev_status, SD_DEV_BAD_PAGE);
+        page = -1;
       }
       // a page goes by TMA when it is in range and all 16 of its tokens are valid
       const bool page_full = page >= 0 && (lane + 1) * kPage <= valid;
@@ -418,22 +419,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       for (int pi = 0; pi < 8; ++pi) {
         if (tma_mask & (1u << pi)) continue;
         const int pg = __shfl_sync(0xffffffffu, page, pi);
-        stage_rows(dst, kT, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
+        stage_rows(dst, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
           return (pg >= 0 && pi * kPage + slot < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim
                                                         : nullptr;
         }, lane, 32);
       }
       if (tma_mask != 0xffu) fence_async_smem();   // plain copies above: make them visible to the MMA
       __syncwarp();
-      if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask) * (kPage * 512));
+      if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask) * kPageB);
       __syncwarp();
-      // lane l: page l/4, 64-dim block l%4 -- one 16-row x 64-dim box each
-      {
-        const int pi = lane >> 2, blk = lane & 3;
-        const int pg = __shfl_sync(0xffffffffu, page, pi);
-        if (tma_mask & (1u << pi))
-          tma_load_2d(smem_u32(dst + blk * kRegionB + pi * kPage * 128), map, blk * 64, (pg * kHkv + g) * kPage, full);
-      }
+      // lane l < 8: page l of the tile, one 8 KB box
+      if (lane < 8 && ((tma_mask >> lane) & 1u))
+        tma_load_page(smem_u32(dst + lane * kPageB), map, (page * kHkv + g) * 2, full);
       if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
     }
   } else {
@@ -464,11 +461,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }, [&](int vr, int chunk) -> uint8_t* {
       if (vr < NQ) return sQ + tile_off(NQ, vr, chunk);
       vr -= NQ;
-      return (vr < k_rows ? sK + tile_off(kT, vr, chunk) : sV + tile_off(kT, vr - k_rows, chunk));
+      return (vr < k_rows ? sK + kv_off(vr, chunk) : sV + kv_off(vr - k_rows, chunk));
     }, ct, nct);
     if (has_draft) {
       for (int i = ct; i < (kT - n_nodes) * 32; i += nct)
-        *reinterpret_cast<uint4*>(sV + tile_off(kT, n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
       // Ancestor set of node ct by walking its root path, then (after the
       // compute warps' barrier) the descendant set of node ct as the
       // transpose: no shared-memory atomics.
@@ -526,9 +523,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kDim / 16; ++kk) {
-              // K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
+              // A = K, K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
+              // B = Q^T, K-major, block-major: 64-dim blocks NQ * 128 B apart, 8-row groups 1 KB apart
               const uint32_t off = (kk & 3) * 32;
-              umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * kRegionB + off, 16, 1024),
+              umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * 1024 + off, 16, kGroupB),
                    sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024),
                    kIdescQK, kk > 0 ? 1u : 0u);
             }
@@ -554,7 +552,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
-                umma(tmem + kColO + h * NQ, sw128_desc(v_addr + 2 * h * kRegionB + j * 2048, kRegionB, 1024),
+                umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
                      pb, kIdescPV, acc);
               }
               // l += 1^T . P^T: every 8-row group of the all-ones operand aliases the same 1 KB
@@ -651,22 +649,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
       };
 
-      // Pass 1: does any score exceed its column's running maximum by more than 2^8?
-      float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Pass 1: does any score exceed its column's running maximum by more
+      // than 2^8?  (The first tile always sets the maxima.)
+      bool slow = true;
+      if (i > 0) {
+        float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int g32 = 0; g32 < NG; ++g32) {
-        float v[32], mm[32];
-        load_scores(g32, v);
-        load_cols(sm->m, g32 * 32, mm);
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32], mm[32];
+          load_scores(g32, v);
+          load_cols(sm->m, g32 * 32, mm);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v[e] - mm[e]);
+          for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v[e] - mm[e]);
+        }
+        const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
+        if (lane == 0) sm->flag[i & 1][sw] = 0;
+        __syncwarp();
+        if (__any_sync(0xffffffffu, dmax > kThresh) && lane == 0) sm->flag[i & 1][sw] = 1;
+        if (!group_sync()) break;
+        slow = (sm->flag[i & 1][0] | sm->flag[i & 1][1] | sm->flag[i & 1][2] | sm->flag[i & 1][3]) != 0;
       }
-      const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
-      if (lane == 0) sm->flag[i & 1][sw] = 0;
-      __syncwarp();
-      if (__any_sync(0xffffffffu, dmax > kThresh) && lane == 0) sm->flag[i & 1][sw] = 1;
-      if (!group_sync()) break;
-      const bool slow = (sm->flag[i & 1][0] | sm->flag[i & 1][1] | sm->flag[i & 1][2] | sm->flag[i & 1][3]) != 0;
       bool pv_waited = false;
       if (slow) {
         // exact column maxima of this tile, new running maxima and rescale factors
@@ -749,9 +751,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // Each thread owns dims `row` and 128 + `row` of every query column.  The
     // column sums l sit in every tensor-memory lane, so each thread reads the
     // ones it needs beside its O^T values.  The normalised rows are staged in
-    // the idle K/V tiles (256 values per query column, columns of one node
-    // adjacent, as are their output rows) and leave with one bulk copy per
-    // node: far fewer memory requests than per-thread stores.
+    // the idle K/V tiles (256 values per query column) and leave as 16-byte
+    // vector stores, far fewer memory requests than per-thread scalar stores.
     if (!*(volatile int*)&sm->abort && mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
       tc_fence_after();
       const bool direct = nsplit == 1;
@@ -781,7 +782,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
         }
       }
-      fence_async_smem();   // the staged rows are read by the bulk copies (async proxy)
+
       // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
       if (sw * 32 < rows) {
         float l32[32];
@@ -806,15 +807,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
         }
       }
-      if (group_sync() && sw == 0) {
-        const int row_b = direct ? kDim * 2 : kDim * 4;
-        for (int n = lane; n < n_nodes; n += 32) {
-          const size_t orow0 = (size_t)(q0 + n) * kHq + head0;
-          void* dst = direct ? static_cast<void*>(p.out + orow0 * kDim)
-                             : static_cast<void*>(p.o_part + (part0 + orow0) * kDim);
-          bulk_store(dst, smem_u32(sK + n * hpc * row_b), (uint32_t)(hpc * row_b));
+      if (group_sync()) {
+        // 16-byte chunks of the staged rows to their output rows, 4 in flight
+        // per thread (the last round repeats the final chunk instead of branching)
+        const int cpr_log2 = direct ? 5 : 6;             // chunks per row: 512 or 1024 bytes
+        const int total = rows << cpr_log2;
+        uint8_t* gbase = direct ? reinterpret_cast<uint8_t*>(p.out)
+                                : reinterpret_cast<uint8_t*>(p.o_part + part0 * kDim);
+        const int t128 = sw * 32 + lane;
+        for (int c0 = t128; c0 - t128 < total; c0 += 4 * 128) {
+          uint4 v[4];
+          int cc[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            cc[u] = min(c0 + u * 128, total - 1);
+            v[u] = *reinterpret_cast<const uint4*>(sK + cc[u] * 16);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = cc[u] >> cpr_log2;
+            const size_t off = ((size_t)sm->outrow[q] << (cpr_log2 + 4)) + ((cc[u] & ((1 << cpr_log2) - 1)) << 4);
+            *reinterpret_cast<uint4*>(gbase + off) = v[u];
+          }
         }
-        bulk_commit_and_wait();
       }
     }
   }
@@ -843,17 +858,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The cache as [pool pages * 4 KV heads * 16 slots] rows of 256 bf16; a box
-// of 16 rows x 64 dims (one page of one head, one 64-dim block) lands as 16
-// rows x 128 B with the 128-byte swizzle.
+// The cache viewed as 4-D: x = dim within a 64-dim block (contiguous),
+// y = slot within an 8-slot half page (512 B apart), z = 64-dim block (128 B
+// apart), w = half page of one KV head ((page * 4 + head) * 2 + half, 4 KB
+// apart).  A box of {64, 8, 4, 2} is one page of one head (8 KB) and lands
+// as [half][block][8 slots][128 B] with the 128-byte swizzle: two 8-row
+// groups of the group-major K/V tile.
 bool cache_map(CUtensorMap* map, const void* cache, int pool_pages) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)pool_pages * kHkv * kPage};
-  cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
+  cuuint64_t dims[4] = {64, 8, 4, (cuuint64_t)pool_pages * kHkv * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, 128, (cuuint64_t)kDim * 2 * 8};
+  cuuint32_t box[4] = {64, 8, 4, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
