@@ -61,6 +61,7 @@ constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 cloc
 enum Bar { K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE, GROUP, NUM_BARS };
 
 constexpr int kCols = 128;   // per-column arrays padded to whole 32-column groups
+constexpr int kMaxStageRows = kTcMaxNQ + 2 * kMaxNodes;   // Q^T rows + the draft block's K and V rows
 
 // Per-column arrays first: each is read with 16-byte vector loads.
 struct Small {
@@ -72,6 +73,11 @@ struct Small {
   unsigned long long anc[kMaxNodes];    // bit r of anc[n]: draft node r is node n or one of its ancestors
   unsigned long long desc[kMaxNodes];   // bit n of desc[r]: the same relation, transposed
   int par[kMaxNodes];
+  // Row copies of the staging pass: source row (null: zeros), byte offset of
+  // the row's chunk 0 in the dynamic shared memory, and its 64-dim block stride.
+  const __nv_bfloat16* rsrc[kMaxStageRows];
+  uint32_t rdst[kMaxStageRows];
+  uint32_t rblk[kMaxStageRows];
   int flag[2][4];
   uint32_t tmem;
   int abort;
@@ -81,6 +87,8 @@ static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &
                   offsetof(Small, outrow) % 16 == 0,
               "per-column arrays must be 16-byte aligned");
 static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + kOnesB + sizeof(Small) <= 232448,
+              "the widest tile configuration must fit in 227 KB of shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -207,11 +215,6 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 
-// Byte offset of 16-byte chunk c (0..31) of row r in the block-major Q^T
-// tile of `rows` rows: 64-dim block c/8, row r, swizzled chunk (c%8) ^ (r%8).
-__device__ __forceinline__ uint32_t tile_off(int rows, int r, int c) {
-  return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 // Byte offset of 16-byte chunk c (0..31) of token row r in a group-major
 // K/V tile: 8-row group r/8 (4 KB), 64-dim block c/8 (1 KB), row r%8,
 // swizzled chunk (c%8) ^ (r%8).  A page's 16 rows are 8 contiguous KB.
@@ -248,30 +251,6 @@ __device__ __forceinline__ void stage_rows(uint8_t* base, int r0, int nrows, Src
       const int task = t0 + u * nthreads;
       if (task < tasks) *reinterpret_cast<uint4*>(base + kv_off(r0 + (task >> 5), task & 31)) = v[u];
     }
-  }
-}
-
-// Copy `nrows` rows of 256 bf16 into group-major tiles: row i comes from
-// src_of(i) (zeros when null) and lands at the shared-memory byte offset
-// dst_of(i, chunk).  `nthreads` threads starting at `t` share the 16-byte
-// chunks, up to 16 loads in flight per thread; the last round re-copies the
-// final chunk instead of branching, so the unrolled copies stay independent.
-template <typename SrcFn, typename DstFn>
-__device__ __forceinline__ void stage_rows_fast(int nrows, SrcFn src_of, DstFn dst_of, int t, int nthreads) {
-  constexpr int U = 16;
-  const int tasks = nrows * 32;
-  for (int t0 = t; t0 - t < tasks; t0 += nthreads * U) {
-    uint4 v[U];
-    uint8_t* dst[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int task = min(t0 + u * nthreads, tasks - 1);
-      const __nv_bfloat16* src = src_of(task >> 5);
-      v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + (task & 31)) : make_uint4(0, 0, 0, 0);
-      dst[u] = dst_of(task >> 5, task & 31);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dst[u]) = v[u];
   }
 }
 
@@ -385,7 +364,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   for (int i = tid; i < kOnesB / 16; i += kThreads)   // bf16 1.0 = 0x3F80
     reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   if (has_draft && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];   // one load each; the walk below is in shared memory
-  __syncthreads();  // mbarriers and per-column arrays ready
+  // The staging pass's row table: Q^T (K-major, block-major): column q = node
+  // * hpc + head-in-part (the hpc heads of a node are adjacent rows of q),
+  // zeros past `rows`; the draft CTA adds its block as the K and V tiles
+  // (group-major), node t = token row t.
+  const int n_stage = NQ + (has_draft ? 2 * n_nodes : 0);
+  for (int r = tid; r < n_stage; r += kThreads) {
+    const __nv_bfloat16* src;
+    uint32_t dst, blk;
+    if (r < NQ) {
+      src = r < rows ? p.q + ((size_t)(q0 + r / hpc) * kHq + head0 + r % hpc) * kDim : nullptr;
+      dst = (uint32_t)(sQ - dyn_smem) + r * 128;
+      blk = NQ * 128;
+    } else {
+      const bool is_v = r >= NQ + n_nodes;
+      const int t = r - NQ - (is_v ? n_nodes : 0);
+      src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + t) * kHkv + g) * kDim;
+      dst = (uint32_t)((is_v ? sV : sK) - dyn_smem) + (t >> 3) * kGroupB + (t & 7) * 128;
+      blk = 1024;
+    }
+    sm->rsrc[r] = src;
+    sm->rdst[r] = dst;
+    sm->rblk[r] = blk;
+  }
+  __syncthreads();  // mbarriers, per-column arrays and the row table ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
 
@@ -439,32 +441,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // (and split 0's draft block, tile 0) and allocate tensor memory.
   {
     const int ct = tid - 32, nct = 5 * 32;
-    // One pass of row copies with every load in flight at once:
-    //   Q^T (K-major): column q = node * hpc + head-in-part (the hpc heads of
-    //   a node are adjacent rows of q), zero past `rows`;
-    //   draft CTA only: the draft block as the K and V tile, node t = token
-    //   row t.  K rows past the block are left stale (their scores are
-    //   masked); V rows past it are zeroed below (P^T is 0 there, and 0 times
-    //   stale shared memory could be NaN).
-    const int k_rows = has_draft ? n_nodes : 0;
-    const float inv_hpc = 1.0f / (float)hpc;
-    const __nv_bfloat16* q_base = p.q + ((size_t)q0 * kHq + head0) * kDim;
-    stage_rows_fast(NQ + 2 * k_rows, [&](int vr) -> const __nv_bfloat16* {
-      if (vr < NQ) {
-        const int node = __float2int_rz(((float)vr + 0.5f) * inv_hpc);   // vr / hpc, exact for vr < 2^20
-        return vr < rows ? q_base + (size_t)(node * kHq + (vr - node * hpc)) * kDim : nullptr;
+    // One pass of row copies with every load in flight at once (up to 16
+    // per thread); the last round repeats the final chunk instead of
+    // branching, so the unrolled copies stay independent.
+    {
+      constexpr int U = 16;
+      const int tasks = n_stage * 32;
+      for (int t0 = ct; t0 - ct < tasks; t0 += nct * U) {
+        uint4 v[U];
+        uint32_t d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int task = min(t0 + u * nct, tasks - 1);
+          const int r = task >> 5, c = task & 31;
+          const __nv_bfloat16* src = sm->rsrc[r];
+          const uint32_t off = sm->rdst[r];
+          v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0, 0, 0, 0);
+          d[u] = off + (c >> 3) * sm->rblk[r] + (((c & 7) ^ ((off >> 7) & 7)) << 4);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dyn_smem + d[u]) = v[u];
       }
-      vr -= NQ;
-      const __nv_bfloat16* base = vr < k_rows ? p.k_new : p.v_new;
-      vr = vr < k_rows ? vr : vr - k_rows;
-      return base + ((size_t)(q0 + vr) * kHkv + g) * kDim;
-    }, [&](int vr, int chunk) -> uint8_t* {
-      if (vr < NQ) return sQ + tile_off(NQ, vr, chunk);
-      vr -= NQ;
-      return (vr < k_rows ? sK + kv_off(vr, chunk) : sV + kv_off(vr - k_rows, chunk));
-    }, ct, nct);
+    }
     if (has_draft) {
-      for (int i = ct; i < (kT - n_nodes) * 32; i += nct)
+      // V rows from the block's end to the next 16-row boundary: the draft
+      // tile's PV product stops there, and P^T is 0 on these rows but 0 times
+      // stale shared memory could be NaN.  (S^T rows past the block are masked.)
+      const int v_end = (n_nodes + 15) & ~15;
+      for (int i = ct; i < (v_end - n_nodes) * 32; i += nct)
         *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
       // Ancestor set of node ct by walking its root path, then (after the
       // compute warps' barrier) the descendant set of node ct as the
@@ -544,19 +548,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             ++pf;
             if (!draft) ++vf;
             tc_fence_after();
+            // O^T += V^T . P^T and l += 1^T . P^T over the first `steps` 16-token steps
+            auto issue_pv = [&](const int steps) {
 #pragma unroll
-            for (int j = 0; j < kT / 16; ++j) {
-              const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
-              // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
-              const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
+              for (int j = 0; j < steps; ++j) {
+                const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
+                // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
+                const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
-                umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
-                     pb, kIdescPV, acc);
+                for (int h = 0; h < 2; ++h) {
+                  // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
+                  umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
+                       pb, kIdescPV, acc);
+                }
+                // every 8-row group of the all-ones operand aliases the same 1 KB
+                umma(tmem + kColL, sw128_desc(ones_addr, 16, 0), pb, kIdescL, acc);
               }
-              // l += 1^T . P^T: every 8-row group of the all-ones operand aliases the same 1 KB
-              umma(tmem + kColL, sw128_desc(ones_addr, 16, 0), pb, kIdescL, acc);
+            };
+            if (draft) {
+              issue_pv((n_nodes + 15) >> 4);   // the draft tile holds n_nodes token rows
+            } else {
+              issue_pv(kT / 16);
             }
             umma_commit(bar(V_EMPTY));
             umma_commit(bar(O_DONE));

@@ -86,17 +86,21 @@ class Workload:
 
 
 # The five workloads: name -> parameters.
+# The seeds of the replayed workloads are chosen so that their one planted
+# step accepts the recipe's mean length (within 0.5 over 400 seeds: 4.13 for
+# the 8-chain at p = 0.8, 6.0 for the 22-node trees at p = 0.85, 2.8 mean over
+# the batch of 4-chains), so that accepted tokens per step are typical.
 CONFIGS = {
     "tiny_chain_ctx512": dict(batch=1, layers=1, ctx=512, tree="chain", K=4, vocab=4096,
                               p=0.8, seed=0, table="identity"),
     "chain8_ctx4k": dict(batch=1, layers=16, ctx=4096, tree="chain", K=8, vocab=151936,
-                         p=0.8, seed=1, table="permuted"),
+                         p=0.8, seed=12, table="permuted"),
     "ddtree22_ctx32k": dict(batch=1, layers=16, ctx=32768, tree="ddtree", budget=22,
-                            vocab=151936, p=0.85, seed=2, table="permuted"),
+                            vocab=151936, p=0.85, seed=3, table="permuted"),
     "conc8_chain4_ragged": dict(batch=8, layers=16, ctx=(1024, 16384), tree="chain", K=4,
                                 vocab=151936, p=(0.5, 0.9), seed=3, table="permuted"),
     "ddtree22_ctx128k": dict(batch=1, layers=16, ctx=131072, tree="ddtree", budget=22,
-                             vocab=151936, p=0.85, seed=4, table="permuted"),
+                             vocab=151936, p=0.85, seed=5, table="permuted"),
 }
 
 
