@@ -84,7 +84,7 @@ SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
 size_t attn_workspace(const SplitPlan& pl, const BatchDesc& bd) {
   if (pl.nsplit <= 1) return 0;
   const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
-  return align_up(rows * kDim * sizeof(float)) + align_up(rows * sizeof(float));
+  return align_up(rows * kDim * sizeof(__nv_bfloat16)) + align_up(rows * sizeof(float));
 }
 
 sd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SD_OK : SD_ERR_CUDA; }
@@ -148,8 +148,8 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
   p.num_splits = pl.nsplit;
   if (need > 0) {
     const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
-    p.o_part = static_cast<float*>(workspace);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(float)));
+    p.o_part = static_cast<__nv_bfloat16*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(__nv_bfloat16)));
   }
   return cuda_status(launch_attn_tc(p, bd, static_cast<cudaStream_t>(stream)));
 }

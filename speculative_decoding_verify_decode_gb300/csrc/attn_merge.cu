@@ -1,6 +1,6 @@
 // Log-sum-exp merge of split-KV partial attention outputs.
 //
-// Every split of a sequence wrote its normalised partial output o_s (fp32)
+// Every split of a sequence wrote its normalised partial output o_s (bf16)
 // and its base-2 log-sum-exp lse_s.  With M = max_s lse_s the merged result
 // is o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) and
 // lse = M + log2 sum_s 2^(lse_s - M) (reported in natural log).  Sequences
@@ -11,6 +11,10 @@
 namespace sdv {
 namespace {
 
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -18,7 +22,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // One 256-thread block per (node row, query head): four groups of 64
 // threads each take every fourth split, thread t of a group owning dims
-// 4t..4t+3.  A thread issues the loads of up to kBatch of its splits before
+// 4t..4t+3 (8 bytes of each partial row).  A thread issues the loads of up to kBatch of its splits before
 // it uses any (one round of memory latency for up to 4 * kBatch splits); the
 // groups' sums are added in shared memory.  The split weights use the
 // block-wide maximum of the split LSEs.
@@ -49,13 +53,13 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   const int grp = tid >> 6, t = tid & 63;
   // first batch of this thread's splits, in flight during the max reduction
   float w[kBatch];
-  float4 o[kBatch];
+  uint2 o[kBatch];   // 4 bf16
 #pragma unroll
   for (int k = 0; k < kBatch; ++k) {
     const int s = grp + k * kMergeGroups;
     const size_t row = (size_t)min(s, ns - 1) * stride + row0;
     w[k] = s < ns ? p.lse_part[row] : -INFINITY;
-    o[k] = reinterpret_cast<const float4*>(p.o_part + row * kDim)[t];
+    o[k] = reinterpret_cast<const uint2*>(p.o_part + row * kDim)[t];
   }
   float mx = -INFINITY;
   for (int s = tid; s < ns; s += kMergeThreads) mx = fmaxf(mx, p.lse_part[s * stride + row0]);
@@ -71,8 +75,9 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const float wk = fast_exp2(w[k] - mx);   // 0 for the padding entries (w = -inf)
+      const float2 lo = unpack_bf16(o[k].x), hi = unpack_bf16(o[k].y);
       den += wk;
-      acc.x += wk * o[k].x; acc.y += wk * o[k].y; acc.z += wk * o[k].z; acc.w += wk * o[k].w;
+      acc.x += wk * lo.x; acc.y += wk * lo.y; acc.z += wk * hi.x; acc.w += wk * hi.y;
     }
     base += kBatch * kMergeGroups;
     if (base >= ns) break;
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
       const int s = base + grp + k * kMergeGroups;
       const size_t row = (size_t)min(s, ns - 1) * stride + row0;
       w[k] = s < ns ? p.lse_part[row] : -INFINITY;
-      o[k] = reinterpret_cast<const float4*>(p.o_part + row * kDim)[t];
+      o[k] = reinterpret_cast<const uint2*>(p.o_part + row * kDim)[t];
     }
   }
   if (grp > 0) {

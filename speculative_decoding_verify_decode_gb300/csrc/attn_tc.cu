@@ -51,7 +51,6 @@ constexpr int kT = 128;                 // tokens per tile
 constexpr int kGroupB = 4096;           // 8 token rows x 4 dim blocks x 128 B
 constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 256 dims
 constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
-constexpr int kOnesB = 1024;            // the all-ones operand: 8 rows x 128 B
 constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
 constexpr int kThreads = 224;
 constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
@@ -68,10 +67,10 @@ struct Small {
   float m[kCols];
   float alpha[kCols];
   float red[4][kCols];
+  float lsum[4][kCols];   // per softmax warp: column sums of P over its 32 token rows
   int outrow[kCols];    // output row (node row * 24 + head) of each query column (-1: padding)
   uint64_t bar[NUM_BARS];
   unsigned long long anc[kMaxNodes];    // bit r of anc[n]: draft node r is node n or one of its ancestors
-  unsigned long long desc[kMaxNodes];   // bit n of desc[r]: the same relation, transposed
   int par[kMaxNodes];
   // Row copies of the staging pass: source row (null: zeros), byte offset of
   // the row's chunk 0 in the dynamic shared memory, and its 64-dim block stride.
@@ -83,11 +82,11 @@ struct Small {
   int abort;
 };
 static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &&
-                  offsetof(Small, red) % 16 == 0 &&
+                  offsetof(Small, red) % 16 == 0 && offsetof(Small, lsum) % 16 == 0 &&
                   offsetof(Small, outrow) % 16 == 0,
               "per-column arrays must be 16-byte aligned");
 static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
-static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + kOnesB + sizeof(Small) <= 232448,
+static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + sizeof(Small) <= 232448,
               "the widest tile configuration must fit in 227 KB of shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -295,8 +294,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   constexpr int NG = (NQ + 31) / 32;          // 32-column groups
   constexpr int NATOM = (NQ + 63) / 64;       // 64-column atoms of the P^T tile
   constexpr int kQB = NQ * 512;               // Q^T tile: 4 blocks of NQ rows x 128 B
-  constexpr uint32_t kColS0 = 0, kColO = 2 * NQ, kColL = 4 * NQ;   // tensor-memory columns
-  static_assert(5 * NQ <= 512, "tensor memory holds 2 S^T, 2 O^T halves and l");
+  constexpr uint32_t kColS0 = 0, kColO = 2 * NQ;   // tensor-memory columns
+  static_assert(4 * NQ <= 512, "tensor memory holds 2 S^T and 2 O^T halves");
   // The kernel declares no static shared memory, so the dynamic window starts
   // at a 1024-byte boundary (required by the 128-byte swizzle atoms); indexing
   // it directly keeps every access a shared-space one.
@@ -305,8 +304,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   uint8_t* sK = sQ + kQB;
   uint8_t* sV = sK + kTileB;
   uint8_t* sP = sV + kTileB;
-  uint8_t* sOnes = sP + NATOM * kAtomB;       // 1 KB of bf16 1.0: the all-ones operand
-  Small* sm = reinterpret_cast<Small*>(sOnes + kOnesB);
+  Small* sm = reinterpret_cast<Small*>(sP + NATOM * kAtomB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bid = blockIdx.x;
@@ -359,37 +357,76 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   for (int q = tid; q < kCols; q += kThreads) {
     sm->m[q] = q < NQ ? -INFINITY : 0.f;
+    sm->alpha[q] = 1.f;
     sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
   }
-  for (int i = tid; i < kOnesB / 16; i += kThreads)   // bf16 1.0 = 0x3F80
-    reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   if (has_draft && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];   // one load each; the walk below is in shared memory
-  // The staging pass's row table: Q^T (K-major, block-major): column q = node
-  // * hpc + head-in-part (the hpc heads of a node are adjacent rows of q),
-  // zeros past `rows`; the draft CTA adds its block as the K and V tiles
-  // (group-major), node t = token row t.
-  const int n_stage = NQ + (has_draft ? 2 * n_nodes : 0);
-  for (int r = tid; r < n_stage; r += kThreads) {
-    const __nv_bfloat16* src;
-    uint32_t dst, blk;
-    if (r < NQ) {
-      src = r < rows ? p.q + ((size_t)(q0 + r / hpc) * kHq + head0 + r % hpc) * kDim : nullptr;
-      dst = (uint32_t)(sQ - dyn_smem) + r * 128;
-      blk = NQ * 128;
-    } else {
-      const bool is_v = r >= NQ + n_nodes;
-      const int t = r - NQ - (is_v ? n_nodes : 0);
-      src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + t) * kHkv + g) * kDim;
-      dst = (uint32_t)((is_v ? sV : sK) - dyn_smem) + (t >> 3) * kGroupB + (t & 7) * 128;
-      blk = 1024;
-    }
-    sm->rsrc[r] = src;
-    sm->rdst[r] = dst;
-    sm->rblk[r] = blk;
-  }
-  __syncthreads();  // mbarriers, per-column arrays and the row table ready
+  __syncthreads();  // mbarriers and per-column arrays ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
+
+  // Staging of the operands that do not come by TMA, by `nthr` threads
+  // (index t): Q^T (K-major, block-major; column q = node * hpc +
+  // head-in-part, the hpc heads of a node being adjacent rows of q; zeros past
+  // `rows`) and, in the draft CTA, the draft block as the K and V tiles
+  // (group-major; node t = token row t).  A row table (source, destination,
+  // block stride) is built first, then one pass of 16-byte copies with up to
+  // 16 loads in flight per thread; the last round repeats the final chunk
+  // instead of branching, so the unrolled copies stay independent.
+  auto stage_operands = [&](const int t, const int nthr, const bool all_warps) {
+    const float inv_hpc = 1.0f / (float)hpc;
+    const int n_stage = NQ + (has_draft ? 2 * n_nodes : 0);
+    for (int r = t; r < n_stage; r += nthr) {
+      const __nv_bfloat16* src;
+      uint32_t dst, blk;
+      if (r < NQ) {
+        const int node = __float2int_rz(((float)r + 0.5f) * inv_hpc);   // r / hpc, exact for r < 2^20
+        src = r < rows ? p.q + ((size_t)(q0 + node) * kHq + head0 + r - node * hpc) * kDim : nullptr;
+        dst = (uint32_t)(sQ - dyn_smem) + r * 128;
+        blk = NQ * 128;
+      } else {
+        const bool is_v = r >= NQ + n_nodes;
+        const int tok = r - NQ - (is_v ? n_nodes : 0);
+        src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + tok) * kHkv + g) * kDim;
+        dst = (uint32_t)((is_v ? sV : sK) - dyn_smem) + (tok >> 3) * kGroupB + (tok & 7) * 128;
+        blk = 1024;
+      }
+      sm->rsrc[r] = src;
+      sm->rdst[r] = dst;
+      sm->rblk[r] = blk;
+    }
+    if (all_warps) __syncthreads();
+    else asm volatile("bar.sync 3, 160;" ::: "memory");   // the five compute warps
+    constexpr int U = 16;
+    const int tasks = n_stage * 32;
+    for (int t0 = t; t0 - t < tasks; t0 += nthr * U) {
+      uint4 v[U];
+      uint32_t d[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int task = min(t0 + u * nthr, tasks - 1);
+        const int r = task >> 5, c = task & 31;
+        const __nv_bfloat16* src = sm->rsrc[r];
+        const uint32_t off = sm->rdst[r];
+        v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0, 0, 0, 0);
+        d[u] = off + (c >> 3) * sm->rblk[r] + (((c & 7) ^ ((off >> 7) & 7)) << 4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dyn_smem + d[u]) = v[u];
+    }
+  };
+  if (has_draft) {
+    // The draft CTA has no TMA work: all seven warps stage its operands.  V
+    // rows from the block's end to the next 16-row boundary are zeroed (the
+    // draft tile's PV product stops there; P^T is 0 on them, but 0 times stale
+    // shared memory could be NaN).  S^T rows past the block are masked.
+    stage_operands(tid, kThreads, true);
+    const int v_end = (n_nodes + 15) & ~15;
+    for (int i = tid; i < (v_end - n_nodes) * 32; i += kThreads)
+      *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();   // plain stores above, read by the tensor core
+    __syncthreads();
+  }
 
   if (warp == kWarpK || warp == kWarpV) {
     // ------------------------------------------------------------ TMA producers (K or V)
@@ -440,58 +477,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // While the producers fetch the first tiles, these five warps stage Q^T
   // (and split 0's draft block, tile 0) and allocate tensor memory.
   {
-    const int ct = tid - 32, nct = 5 * 32;
-    // One pass of row copies with every load in flight at once (up to 16
-    // per thread); the last round repeats the final chunk instead of
-    // branching, so the unrolled copies stay independent.
-    {
-      constexpr int U = 16;
-      const int tasks = n_stage * 32;
-      for (int t0 = ct; t0 - ct < tasks; t0 += nct * U) {
-        uint4 v[U];
-        uint32_t d[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int task = min(t0 + u * nct, tasks - 1);
-          const int r = task >> 5, c = task & 31;
-          const __nv_bfloat16* src = sm->rsrc[r];
-          const uint32_t off = sm->rdst[r];
-          v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0, 0, 0, 0);
-          d[u] = off + (c >> 3) * sm->rblk[r] + (((c & 7) ^ ((off >> 7) & 7)) << 4);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dyn_smem + d[u]) = v[u];
-      }
-    }
-    if (has_draft) {
-      // V rows from the block's end to the next 16-row boundary: the draft
-      // tile's PV product stops there, and P^T is 0 on these rows but 0 times
-      // stale shared memory could be NaN.  (S^T rows past the block are masked.)
-      const int v_end = (n_nodes + 15) & ~15;
-      for (int i = ct; i < (v_end - n_nodes) * 32; i += nct)
-        *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
-      // Ancestor set of node ct by walking its root path, then (after the
-      // compute warps' barrier) the descendant set of node ct as the
-      // transpose: no shared-memory atomics.
-      if (ct < n_nodes) {
-        unsigned long long a = 1ull << ct;
-        bool ok = ct == 0 ? sm->par[0] == -1 : true;
-        for (int u = ct; ok && u > 0;) {
-          const int pu = sm->par[u];
-          ok = pu >= 0 && pu < u;
-          if (ok) a |= 1ull << pu;
-          u = pu;
-        }
-        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << ct; }
-        sm->anc[ct] = a;
-      }
-      asm volatile("bar.sync 2, 160;" ::: "memory");   // the five compute warps of the draft CTA
-      if (ct < n_nodes) {
-        unsigned long long d = 0ull;
-        for (int n = ct; n < n_nodes; ++n) d |= ((sm->anc[n] >> ct) & 1ull) << n;
-        sm->desc[ct] = d;
-      }
-    }
+    const int ct = tid - 32;
+    if (!has_draft) stage_operands(ct, 5 * 32, false);
     if (warp == kWarpMma) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -507,9 +494,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t kIdescQK = f16_idesc(128, NQ, 0, 0);
       constexpr uint32_t kIdescPV = f16_idesc(128, NQ, 1, 1);
-      constexpr uint32_t kIdescL = f16_idesc(128, NQ, 0, 1);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
-      const uint32_t ones_addr = smem_u32(sOnes);
       int kf = 0, vf = 0, pf = 0;
       int sfree[2] = {0, 0};
       int qk_next = 0, pv_next = 0;
@@ -548,7 +533,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             ++pf;
             if (!draft) ++vf;
             tc_fence_after();
-            // O^T += V^T . P^T and l += 1^T . P^T over the first `steps` 16-token steps
+            // O^T += V^T . P^T over the first `steps` 16-token steps
             auto issue_pv = [&](const int steps) {
 #pragma unroll
               for (int j = 0; j < steps; ++j) {
@@ -561,8 +546,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                   umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
                        pb, kIdescPV, acc);
                 }
-                // every 8-row group of the all-ones operand aliases the same 1 KB
-                umma(tmem + kColL, sw128_desc(ones_addr, 16, 0), pb, kIdescL, acc);
               }
             };
             if (draft) {
@@ -611,7 +594,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         w[4 * k] = t.x; w[4 * k + 1] = t.y; w[4 * k + 2] = t.z; w[4 * k + 3] = t.w;
       }
     };
-    for (int i = 0; i < n_tiles; ++i) {
+    // Column sums of P, from the bf16 P^T tile this warp wrote (the same
+    // rounded weights the PV product multiplies V with): lane L sums columns
+    // 64a + 8(L%8) .. +7 of atom a over token rows 32 * quarter + L/8 + 4k,
+    // k < 8; the warp's lanes and the four warps are added in the epilogue.
+    float csum[NATOM][8];
+#pragma unroll
+    for (int a = 0; a < NATOM; ++a)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) csum[a][j] = 0.f;
+    const int cs_chunk = lane & 7;
+    // Draft CTA: the tree masks, built while the QK product runs.  Node
+    // `row` walks its root path (its ancestor set), then, after the group
+    // barrier, gathers its descendant set: bit n set when node n has `row` on
+    // its root path (itself included).
+    unsigned long long my_desc = 0ull;
+    bool masks_ok = true;
+    if (has_draft) {
+      if (row < n_nodes) {
+        unsigned long long a = 1ull << row;
+        bool ok = row == 0 ? sm->par[0] == -1 : true;
+        for (int u = row; ok && u > 0;) {
+          const int pu = sm->par[u];
+          ok = pu >= 0 && pu < u;
+          if (ok) a |= 1ull << pu;
+          u = pu;
+        }
+        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << row; }
+        sm->anc[row] = a;
+      }
+      masks_ok = group_sync();
+      if (row < n_nodes) {
+        for (int n = row; n < n_nodes; ++n) my_desc |= ((sm->anc[n] >> row) & 1ull) << n;
+      }
+    }
+    for (int i = 0; i < n_tiles && masks_ok; ++i) {
       const int sb = i & 1;
       if (!mbar_spin(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
       tc_fence_after();
@@ -630,7 +647,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         vis[gq] = (!draft_tile && row < valid) ? (ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u)) : 0u;
       }
       if (draft_tile) {
-        unsigned long long d = row < n_nodes ? sm->desc[row] : 0ull;
+        unsigned long long d = my_desc;
         while (d != 0ull) {
           const int n = __ffsll((long long)d) - 1;
           d &= d - 1ull;
@@ -700,13 +717,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           sm->m[q] = mn;
         }
         if (!group_sync()) break;
+#pragma unroll
+        for (int a = 0; a < NATOM; ++a) {
+          const float4 f0 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[0];
+          const float4 f1 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[1];
+          csum[a][0] *= f0.x; csum[a][1] *= f0.y; csum[a][2] *= f0.z; csum[a][3] *= f0.w;
+          csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
+        }
         if (i > 0) {
-          // O^T and l hold earlier tiles: wait for the last PV, then rescale their columns
+          // O^T holds earlier tiles: wait for the last PV, then rescale its columns
           if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
           pv_waited = true;
           tc_fence_after();
 #pragma unroll 1
-          for (int c16 = 0; c16 < 3 * NQ / 16; ++c16) {   // O^T low, O^T high, l
+          for (int c16 = 0; c16 < 2 * NQ / 16; ++c16) {   // O^T low, O^T high
             float v[16];
             const int col = c16 % (NQ / 16) * 16;
             const uint32_t a = tmem + lane_addr + kColO + c16 * 16;
@@ -757,27 +781,74 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL));
+      // Column sums of this tile's P from the rows this warp just wrote, while
+      // the PV product runs (the next tile overwrites P^T only after it ends).
+#pragma unroll
+      for (int a = 0; a < NATOM; ++a) {
+        if (a * 64 + cs_chunk * 8 < NQ) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = quarter * 32 + (lane >> 3) + 4 * k;
+            const uint4 pv = *reinterpret_cast<const uint4*>(sP + a * kAtomB + p_off(r, cs_chunk));
+            const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
+              csum[a][2 * e] += f.x;
+              csum[a][2 * e + 1] += f.y;
+            }
+          }
+        }
+      }
     }
 
     // ------------------------------------------------------------ epilogue
-    // Each thread owns dims `row` and 128 + `row` of every query column.  The
-    // column sums l sit in every tensor-memory lane, so each thread reads the
-    // ones it needs beside its O^T values.  The normalised rows are staged in
-    // the idle K/V tiles (256 values per query column) and leave as 16-byte
-    // vector stores, far fewer memory requests than per-thread scalar stores.
-    if (!*(volatile int*)&sm->abort && mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
+    // Each thread owns dims `row` and 128 + `row` of every query column; the
+    // column sums l are the four warps' partial sums, added from shared
+    // memory.  The normalised bf16 rows (the output, or this split's partial
+    // for the merge) are staged in the idle K/V tiles, 256 values per query
+    // column, and leave as 16-byte vector stores.
+    if (!*(volatile int*)&sm->abort) {
+      // add the warp's four row groups (lanes with the same lane % 8), then
+      // publish this warp's column sums
+#pragma unroll
+      for (int a = 0; a < NATOM; ++a)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 8);
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 16);
+        }
+      if (lane < 8) {
+#pragma unroll
+        for (int a = 0; a < NATOM; ++a) {
+          float4* dst = reinterpret_cast<float4*>(sm->lsum[sw] + a * 64 + lane * 8);
+          dst[0] = make_float4(csum[a][0], csum[a][1], csum[a][2], csum[a][3]);
+          dst[1] = make_float4(csum[a][4], csum[a][5], csum[a][6], csum[a][7]);
+        }
+      }
+    }
+    if (!*(volatile int*)&sm->abort && group_sync() &&
+        mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
       tc_fence_after();
       const bool direct = nsplit == 1;
       const size_t part0 = (size_t)s * bd.total_nodes * kHq;
       const uint32_t t_row = tmem + lane_addr;
-      float* stage_f = reinterpret_cast<float*>(sK);
-      __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(sK);
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sK);
 #pragma unroll 1
       for (int col = 0; col < NQ; col += 16) {
         float lo[16], hi[16], l[16];
         tmem_ld16(t_row + kColO + col, lo);
         tmem_ld16(t_row + kColO + NQ + col, hi);
-        tmem_ld16(t_row + kColL + col, l);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float4 a = reinterpret_cast<const float4*>(sm->lsum[0] + col)[k];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            const float4 b = reinterpret_cast<const float4*>(sm->lsum[w] + col)[k];
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          }
+          l[4 * k] = a.x; l[4 * k + 1] = a.y; l[4 * k + 2] = a.z; l[4 * k + 3] = a.w;
+        }
         tmem_wait_ld();
         // every column is written (padding columns too: the staging area holds
         // NQ rows), so the 16 columns stay independent of each other
@@ -785,47 +856,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         for (int e = 0; e < 16; ++e) {
           const int q = col + e;
           const float inv = __fdividef(1.0f, l[e]);
-          if (direct) {
-            stage_h[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
-            stage_h[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
-          } else {
-            stage_f[q * kDim + row] = lo[e] * inv;
-            stage_f[q * kDim + 128 + row] = hi[e] * inv;
-          }
+          stage[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
+          stage[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
         }
       }
-
       // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
-      if (sw * 32 < rows) {
-        float l32[32];
-        {
-          float a[16], c2[16];
-          tmem_ld16(t_row + kColL + sw * 32, a);
-          tmem_ld16(t_row + kColL + sw * 32 + 16, c2);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) { l32[e] = a[e]; l32[e + 16] = c2[e]; }
-        }
-        float lq = l32[0];
-#pragma unroll
-        for (int e = 1; e < 32; ++e) lq = lane == e ? l32[e] : lq;
-        const int q = sw * 32 + lane;
-        if (q < rows) {
-          const float lse2 = sm->m[q] + fast_log2(lq);
-          if (direct) {
-            if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
-          } else {
-            p.lse_part[part0 + sm->outrow[q]] = lse2;
-          }
+      for (int q = sw * 32 + lane; q < rows; q += 128) {
+        const float lq = sm->lsum[0][q] + sm->lsum[1][q] + sm->lsum[2][q] + sm->lsum[3][q];
+        const float lse2 = sm->m[q] + fast_log2(lq);
+        if (direct) {
+          if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
+        } else {
+          p.lse_part[part0 + sm->outrow[q]] = lse2;
         }
       }
       if (group_sync()) {
-        // 16-byte chunks of the staged rows to their output rows, 4 in flight
-        // per thread (the last round repeats the final chunk instead of branching)
-        const int cpr_log2 = direct ? 5 : 6;             // chunks per row: 512 or 1024 bytes
-        const int total = rows << cpr_log2;
-        uint8_t* gbase = direct ? reinterpret_cast<uint8_t*>(p.out)
-                                : reinterpret_cast<uint8_t*>(p.o_part + part0 * kDim);
+        // 16-byte chunks of the staged 512-byte rows to their output rows, 4 in
+        // flight per thread (the last round repeats the final chunk instead of branching)
+        const int total = rows << 5;
+        uint8_t* gbase = reinterpret_cast<uint8_t*>(direct ? p.out : p.o_part + part0 * kDim);
         const int t128 = sw * 32 + lane;
         for (int c0 = t128; c0 - t128 < total; c0 += 4 * 128) {
           uint4 v[4];
@@ -837,8 +886,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int q = cc[u] >> cpr_log2;
-            const size_t off = ((size_t)sm->outrow[q] << (cpr_log2 + 4)) + ((cc[u] & ((1 << cpr_log2) - 1)) << 4);
+            const size_t off = ((size_t)sm->outrow[cc[u] >> 5] << 9) + ((cc[u] & 31) << 4);
             *reinterpret_cast<uint4*>(gbase + off) = v[u];
           }
         }
@@ -911,7 +959,7 @@ cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnPa
 
 size_t tc_smem_bytes(int nq) {
   const int natom = (nq + 63) / 64;
-  return (size_t)nq * 512 + 2 * (size_t)kTileB + (size_t)natom * kAtomB + kOnesB + sizeof(Small);
+  return (size_t)nq * 512 + 2 * (size_t)kTileB + (size_t)natom * kAtomB + sizeof(Small);
 }
 
 TcPlan tc_plan(int max_nodes) {

@@ -43,7 +43,7 @@ struct AttnParams {
   const int* parents;
   __nv_bfloat16* out;
   float* lse;            // nullable
-  float* o_part;         // [num_splits][total_nodes][24][256]
+  __nv_bfloat16* o_part; // [num_splits][total_nodes][24][256] normalised partial outputs
   float* lse_part;       // [num_splits][total_nodes][24]  (base-2 log-sum-exp)
   int* dev_status;       // nullable
   int max_pages;
