@@ -22,10 +22,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // One 256-thread block per (node row, query head): four groups of 64
 // threads each take every fourth split, thread t of a group owning dims
-// 4t..4t+3 (8 bytes of each partial row).  A thread issues the loads of up to kBatch of its splits before
-// it uses any (one round of memory latency for up to 4 * kBatch splits); the
-// groups' sums are added in shared memory.  The split weights use the
-// block-wide maximum of the split LSEs.
+// 4t..4t+3 (8 bytes of each partial row).  A thread issues the loads of up to
+// kBatch of its splits before it uses any (one round of memory latency for up
+// to 4 * kBatch splits) and keeps its group's running (max, sum, weighted sum)
+// in base 2; the four groups are combined once, through shared memory.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 64;
 constexpr int kBatch = 12;
@@ -46,41 +46,14 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const size_t stride = (size_t)bd.total_nodes * kHq;   // rows between splits
   const size_t row0 = (size_t)r * kHq + head;
-  __shared__ float s_max[kMergeThreads / 32];
-  __shared__ float4 s_acc[kMergeGroups - 1][64];
-  __shared__ float s_den[kMergeGroups - 1];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = tid >> 6, t = tid & 63;
-  // first batch of this thread's splits, in flight during the max reduction
-  float w[kBatch];
-  uint2 o[kBatch];   // 4 bf16
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int s = grp + k * kMergeGroups;
-    const size_t row = (size_t)min(s, ns - 1) * stride + row0;
-    w[k] = s < ns ? p.lse_part[row] : -INFINITY;
-    o[k] = reinterpret_cast<const uint2*>(p.o_part + row * kDim)[t];
-  }
-  float mx = -INFINITY;
-  for (int s = tid; s < ns; s += kMergeThreads) mx = fmaxf(mx, p.lse_part[s * stride + row0]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) s_max[warp] = mx;
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kMergeThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+  __shared__ float4 s_acc[kMergeGroups][64];
+  __shared__ float s_max[kMergeGroups], s_den[kMergeGroups];
+  const int grp = threadIdx.x >> 6, t = threadIdx.x & 63;
+  float mx = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  for (int base = 0;;) {
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const float wk = fast_exp2(w[k] - mx);   // 0 for the padding entries (w = -inf)
-      const float2 lo = unpack_bf16(o[k].x), hi = unpack_bf16(o[k].y);
-      den += wk;
-      acc.x += wk * lo.x; acc.y += wk * lo.y; acc.z += wk * hi.x; acc.w += wk * hi.y;
-    }
-    base += kBatch * kMergeGroups;
-    if (base >= ns) break;
+  for (int base = 0; base < ns; base += kBatch * kMergeGroups) {
+    float w[kBatch];
+    uint2 o[kBatch];   // 4 bf16
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int s = base + grp + k * kMergeGroups;
@@ -88,25 +61,44 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
       w[k] = s < ns ? p.lse_part[row] : -INFINITY;
       o[k] = reinterpret_cast<const uint2*>(p.o_part + row * kDim)[t];
     }
+    float bm = mx;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, w[k]);
+    if (bm > mx) {   // rescale what this group has so far to the new maximum
+      const float a = mx == -INFINITY ? 0.f : fast_exp2(mx - bm);
+      den *= a; acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+      mx = bm;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float wk = w[k] == -INFINITY ? 0.f : fast_exp2(w[k] - mx);   // padding entries weigh 0
+      const float2 a = unpack_bf16(o[k].x), b = unpack_bf16(o[k].y);
+      den += wk;
+      acc.x += wk * a.x; acc.y += wk * a.y; acc.z += wk * b.x; acc.w += wk * b.y;
+    }
   }
-  if (grp > 0) {
-    s_acc[grp - 1][t] = acc;
-    if (t == 0) s_den[grp - 1] = den;
-  }
+  s_acc[grp][t] = acc;
+  if (t == 0) { s_max[grp] = mx; s_den[grp] = den; }
   __syncthreads();
   if (grp > 0) return;
+  float m_all = s_max[0];
 #pragma unroll
-  for (int k = 0; k < kMergeGroups - 1; ++k) {
+  for (int k = 1; k < kMergeGroups; ++k) m_all = fmaxf(m_all, s_max[k]);
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  float d_all = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMergeGroups; ++k) {
+    const float a = s_max[k] == -INFINITY ? 0.f : fast_exp2(s_max[k] - m_all);   // a group may hold no split
     const float4 v = s_acc[k][t];
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    den += s_den[k];
+    d_all += a * s_den[k];
+    sum.x += a * v.x; sum.y += a * v.y; sum.z += a * v.z; sum.w += a * v.w;
   }
-  const float inv = 1.f / den;
+  const float inv = 1.f / d_all;
   uint2 packed;
-  packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+  packed.x = pack_bf16(sum.x * inv, sum.y * inv);
+  packed.y = pack_bf16(sum.z * inv, sum.w * inv);
   reinterpret_cast<uint2*>(p.out + row0 * kDim)[t] = packed;
-  if (p.lse != nullptr && t == 0) p.lse[row0] = (mx + fast_log2(den)) * kLn2;
+  if (p.lse != nullptr && t == 0) p.lse[row0] = (m_all + fast_log2(d_all)) * kLn2;
 }
 
 }  // namespace

@@ -319,6 +319,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // Launched as a programmatic dependent: wait for the previous kernel in the
   // stream before touching global memory, then let the merge kernel's blocks
   // be scheduled (they wait for this grid to finish before reading).
+  // the producers fetch their TMA descriptor while the rest of the prologue runs
+  if ((warp == kWarpK || warp == kWarpV) && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpK ? &tm_k : &tm_v))
+                 : "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Split 0 attends to the draft block alone; split s >= 1 to context tokens
