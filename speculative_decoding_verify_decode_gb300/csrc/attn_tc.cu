@@ -57,7 +57,11 @@ constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 
-enum Bar { K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE, GROUP, NUM_BARS };
+// The V tile moves in two 64-token halves (pages 0-3 and 4-7, each 32 KB
+// contiguous), so that the first half of the next tile loads while the PV
+// product still reads the second half of this one.
+enum Bar { K_FULL, K_EMPTY, V_FULL0, V_FULL1, V_EMPTY0, V_EMPTY1, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE,
+           GROUP, NUM_BARS };
 
 constexpr int kCols = 128;   // per-column arrays padded to whole 32-column groups
 constexpr int kMaxStageRows = kTcMaxNQ + 2 * kMaxNodes;   // Q^T rows + the draft block's K and V rows
@@ -438,7 +442,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     uint8_t* dst = is_k ? sK : sV;
     const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-    const uint32_t full = bar(is_k ? K_FULL : V_FULL), empty = bar(is_k ? K_EMPTY : V_EMPTY);
+    const int nparts = is_k ? 1 : 2;           // K: one 8-page part; V: two 4-page halves
+    const int ppp = 8 / nparts;                 // pages per part
     const int n_ctx = has_draft ? 0 : n_tiles;   // the draft CTA stages its block without TMA
     int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
     for (int i = 0; i < n_ctx; ++i) {
@@ -456,24 +461,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page_full);
       const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      // pages that are partial, missing or out of range: plain copies, zero past the context
-      for (int pi = 0; pi < 8; ++pi) {
-        if (tma_mask & (1u << pi)) continue;
-        const int pg = __shfl_sync(0xffffffffu, page, pi);
-        stage_rows(dst, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
-          return (pg >= 0 && pi * kPage + slot < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim
-                                                        : nullptr;
-        }, lane, 32);
+      for (int part = 0; part < nparts && ok; ++part) {
+        const uint32_t full = bar(is_k ? K_FULL : V_FULL0 + part), empty = bar(is_k ? K_EMPTY : V_EMPTY0 + part);
+        const uint32_t part_mask = ((1u << ppp) - 1u) << (part * ppp);
+        if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        // pages that are partial, missing or out of range: plain copies, zero past the context
+        for (int pi = part * ppp; pi < (part + 1) * ppp; ++pi) {
+          if (tma_mask & (1u << pi)) continue;
+          const int pg = __shfl_sync(0xffffffffu, page, pi);
+          stage_rows(dst, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
+            return (pg >= 0 && pi * kPage + slot < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim
+                                                          : nullptr;
+          }, lane, 32);
+        }
+        if ((tma_mask & part_mask) != part_mask) fence_async_smem();   // plain copies above: visible to the MMA
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask & part_mask) * kPageB);
+        __syncwarp();
+        // lane l: page l of the tile, one 8 KB box
+        if (((part_mask & tma_mask) >> lane) & 1u)
+          tma_load_page(smem_u32(dst + lane * kPageB), map, (page * kHkv + g) * 2, full);
       }
-      if (tma_mask != 0xffu) fence_async_smem();   // plain copies above: make them visible to the MMA
-      __syncwarp();
-      if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask) * kPageB);
-      __syncwarp();
-      // lane l < 8: page l of the tile, one 8 KB box
-      if (lane < 8 && ((tma_mask >> lane) & 1u))
-        tma_load_page(smem_u32(dst + lane * kPageB), map, (page * kHkv + g) * 2, full);
+      if (!ok) break;
       if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
     }
   } else {
@@ -499,7 +510,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       constexpr uint32_t kIdescQK = f16_idesc(128, NQ, 0, 0);
       constexpr uint32_t kIdescPV = f16_idesc(128, NQ, 1, 1);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
-      int kf = 0, vf = 0, pf = 0;
+      int kf = 0, pf = 0, vf0 = 0, vf1 = 0;
+      int pv_half = 0;   // the PV product of a context tile runs in two 64-token halves
       int sfree[2] = {0, 0};
       int qk_next = 0, pv_next = 0;
       long long idle_since = clock64();
@@ -529,18 +541,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             progressed = true;
           }
         }
-        // PV (and the column sums) of the oldest tile whose P^T is written
+        // PV of the oldest tile whose P^T is written, one V half at a time
         if (pv_next < qk_next) {
           const int t = pv_next;
           const bool draft = has_draft && t == 0;
-          if (mbar_test(bar(P_FULL), pf & 1) && (draft || mbar_test(bar(V_FULL), vf & 1))) {
-            ++pf;
-            if (!draft) ++vf;
+          const bool ready = pv_half == 0 ? mbar_test(bar(P_FULL), pf & 1) && (draft || mbar_test(bar(V_FULL0), vf0 & 1))
+                                          : mbar_test(bar(V_FULL1), vf1 & 1);
+          if (ready) {
+            if (pv_half == 0) {
+              ++pf;
+              if (!draft) ++vf0;
+            } else {
+              ++vf1;
+            }
             tc_fence_after();
-            // O^T += V^T . P^T over the first `steps` 16-token steps
-            auto issue_pv = [&](const int steps) {
+            // O^T += V^T . P^T over 16-token steps j0 .. j0 + steps - 1
+            auto issue_pv = [&](const int j0, const int steps) {
 #pragma unroll
-              for (int j = 0; j < steps; ++j) {
+              for (int jj = 0; jj < steps; ++jj) {
+                const int j = j0 + jj;
                 const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
                 // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
                 const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
@@ -553,13 +572,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
               }
             };
             if (draft) {
-              issue_pv((n_nodes + 15) >> 4);   // the draft tile holds n_nodes token rows
+              // the draft tile holds n_nodes <= 64 token rows: all in the first half
+              issue_pv(0, (n_nodes + 15) >> 4);
+              umma_commit(bar(O_DONE));
+              ++pv_next;
+            } else if (pv_half == 0) {
+              issue_pv(0, kT / 32);
+              umma_commit(bar(V_EMPTY0));
+              pv_half = 1;
             } else {
-              issue_pv(kT / 16);
+              issue_pv(kT / 32, kT / 32);
+              umma_commit(bar(V_EMPTY1));
+              umma_commit(bar(O_DONE));
+              pv_half = 0;
+              ++pv_next;
             }
-            umma_commit(bar(V_EMPTY));
-            umma_commit(bar(O_DONE));
-            ++pv_next;
             progressed = true;
           }
         }
