@@ -38,7 +38,11 @@ Readings where the pages are silent (each is also listed in the design notes):
 * argmax ties go to the smallest index; -0.0 equals +0.0; NaN is rejected;
 * among accepted root paths of maximal length, ties go to the
   lexicographically smallest sequence of node indices;
-* A = accepted drafts + 1 (root counts), so an all-rejected step gives A = 1.
+* A = accepted drafts + 1 (root counts), so an all-rejected step gives A = 1;
+* sliding window W [S5 补充测试: attention over the most recent 2,048 KV
+  positions only]: node j sits at position L + depth(j), and a key at position
+  t is visible to it when t > L + depth(j) - W (the W most recent positions,
+  its own included); a draft ancestor n is at position L + depth(n).
 """
 from __future__ import annotations
 
@@ -120,7 +124,7 @@ def attend(qv, keys, values, visible) -> tuple[np.ndarray, float]:
 
 
 def verify_attention(q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, q_indptr, parents,
-                     samples=None):
+                     samples=None, window=None):
     """Tree/causal-masked grouped-query attention of one layer.
 
     q [sumN, 24, D]; k_cache/v_cache [P, 4, 16, D]; k_new/v_new [sumN, 4, D];
@@ -131,7 +135,9 @@ def verify_attention(q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, q_
 
     Returns (o [sumN, 24, D], lse [sumN, 24]) in float64.  With ``samples`` (a
     list of (row, head) pairs) only those entries are computed and the result
-    is (o [S, D], lse [S]).
+    is (o [S, D], lse [S]).  With ``window`` W >= 1 each query sees only the
+    keys at its W most recent positions (node j at position L + depth(j)
+    [S5 补充测试]); None or 0 means the whole context.
     """
     q = np.asarray(q)
     indptr = np.asarray(q_indptr)
@@ -148,7 +154,7 @@ def verify_attention(q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, q_
     lse_out = np.zeros(len(want), dtype=np.float64)
     for (b, g), items in sorted(by_seq_head.items()):
         lo, hi = int(indptr[b]), int(indptr[b + 1])
-        paths, _ = tree_ancestors(np.asarray(parents)[lo:hi])
+        paths, depth = tree_ancestors(np.asarray(parents)[lo:hi])
         L = int(np.asarray(ctx_lens)[b])
         row = np.asarray(page_table)[b]
         keys = np.concatenate([gather_context(k_cache, row, L, g),
@@ -158,8 +164,14 @@ def verify_attention(q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, q_
         for i in items:
             r, h = want[i]
             visible = np.zeros(L + hi - lo, dtype=bool)
-            visible[:L] = True
-            visible[[L + n for n in paths[r - lo]]] = True
+            if window:
+                pos = L + int(depth[r - lo])                 # this query's position
+                first = max(0, pos - int(window) + 1)        # oldest visible position
+                visible[first:L] = True
+                visible[[L + n for n in paths[r - lo] if L + int(depth[n]) >= first]] = True
+            else:
+                visible[:L] = True
+                visible[[L + n for n in paths[r - lo]]] = True
             o_out[i], lse_out[i] = attend(q[r, h, :], keys, vals, visible)
     if samples is not None:
         return o_out, lse_out
