@@ -50,10 +50,14 @@ def attn_bytes_per_layer(w) -> int:
     """Algorithmic bytes of one layer's verify attention.
 
     Context K and V are read once (2 x 4 heads x 256 x 2 B = 4096 B per token),
-    plus Q, the draft K/V, the output and the page-table entries.
+    plus Q, the draft K/V, the output and the page-table entries.  With a
+    sliding window W only the W - 1 most recent context tokens are visible.
     """
-    ctx = int(np.asarray(w.ctx_lens, dtype=np.int64).sum())
-    pages = int(sum((int(L) + 15) // 16 for L in w.ctx_lens))
+    lens = [int(L) for L in w.ctx_lens]
+    if getattr(w, "window", 0):
+        lens = [min(L, w.window - 1) for L in lens]
+    ctx = sum(lens)
+    pages = int(sum((L + 15) // 16 for L in lens))
     n = w.total_nodes
     return ctx * 4096 + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
 
@@ -165,7 +169,7 @@ def run_ours(args, world, rank, local):
     w = synth.make_workload(args.config, device=dev, layers=args.layers or None)
     d = device_inputs(w, dev)
     step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev,
-                      num_splits=args.splits)
+                      num_splits=args.splits, window=w.window)
     run_args = (w.q, w.k_cache, w.v_cache, w.k_new, w.v_new, d["page_table"], d["ctx_lens"], d["parents"],
                 d["draft_tokens"], w.logits)
     step.run(*run_args)                       # eager once: surfaces launch errors early
@@ -257,7 +261,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; Q/K/V ~ N(0,1)/16 bf16, planted-argmax fp32 logits)",
-        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers,
+        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "window": w.window,
                    "ctx_lens": [int(x) for x in w.ctx_lens][:8], "draft_nodes": w.total_nodes,
                    "vocab": w.vocab, "heads": "24q/4kv", "head_dim": 256, "page": 16,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -297,7 +301,7 @@ def cpu_baseline(w, config: str, reps: int = 1) -> dict:
     for _ in range(reps):
         t = time.perf_counter()
         oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
-                                w.ctx_lens, w.q_indptr, w.parents)
+                                w.ctx_lens, w.q_indptr, w.parents, window=w.window or None)
         t_attn.append(time.perf_counter() - t)
         t = time.perf_counter()
         _, lens, paths, _ = oracle.accept(w.q_indptr, w.parents, w.draft_tokens, logits)
@@ -327,7 +331,8 @@ def run_reference(args, world, rank, local):
     return {"metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "vocab": w.vocab},
+            "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "vocab": w.vocab,
+                       "window": w.window},
             "impl": "reference", "cpu_baseline": {**base, "wall_s": wall},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

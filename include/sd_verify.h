@@ -95,6 +95,10 @@ typedef struct sd_shape {
   int max_pages_per_seq;     /* columns of page_table, >= 1 */
   int num_pool_pages;        /* pages in each layer's cache pool, >= 1 */
   int num_splits;            /* split-KV chunks per (sequence, KV head); 0 = choose automatically */
+  int window;                /* sliding window W >= 1: node j (position L + depth(j)) attends only to keys at
+                                positions > L + depth(j) - W, its W most recent ones (own key included);
+                                0 = the whole context.  Source: «如何在单张 RTX 3090 上让 Qwen3.5-27B token
+                                生成速度提升 6 倍», 补充测试 (attention over the most recent 2,048 positions). */
 } sd_shape;
 
 /* Human-readable name of a status code (static string). */

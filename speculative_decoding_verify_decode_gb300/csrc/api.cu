@@ -35,7 +35,8 @@ sd_status check_shape(const sd_shape* s, BatchDesc* bd) {
   if (s == nullptr) return SD_ERR_INVALID_ARG;
   if (s->num_q_heads != kHq || s->num_kv_heads != kHkv || s->head_dim != kDim || s->page_size != kPage)
     return SD_ERR_UNSUPPORTED;
-  if (s->max_pages_per_seq < 1 || s->num_pool_pages < 1 || s->num_splits < 0) return SD_ERR_INVALID_ARG;
+  if (s->max_pages_per_seq < 1 || s->num_pool_pages < 1 || s->num_splits < 0 || s->window < 0)
+    return SD_ERR_INVALID_ARG;
   if ((long long)s->max_pages_per_seq * kPage > (1LL << 30)) return SD_ERR_UNSUPPORTED;
   return fill_batch(s->batch, s->q_indptr_h, bd);
 }
@@ -62,7 +63,10 @@ struct SplitPlan {
 // sequence full), which keeps the last wave short when the lengths are ragged.
 SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
   const int tile = attn_tc_tile();
-  const long long max_ctx = (long long)s->max_pages_per_seq * kPage;
+  long long max_ctx = (long long)s->max_pages_per_seq * kPage;
+  // with a window only the tiles from window_base on are read: at most W - 1 positions plus the
+  // rounding to a tile boundary
+  if (s->window > 0 && (long long)s->window + 2 * tile < max_ctx) max_ctx = (long long)s->window + 2 * tile;
   const long long max_tiles = (max_ctx + tile - 1) / tile;
   long long chunk;
   if (s->num_splits > 0) {
@@ -146,6 +150,7 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
   p.num_pool_pages = shape->num_pool_pages;
   p.chunk = pl.chunk;
   p.num_splits = pl.nsplit;
+  p.window = shape->window;
   if (need > 0) {
     const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
     p.o_part = static_cast<__nv_bfloat16*>(workspace);

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   }
   int L = p.ctx_lens[lo];
   L = L < 0 ? 0 : min(L, p.max_pages * kPage);
-  const int ns = active_splits(L, p.chunk);
+  const int ns = active_splits(L, p.window, kTileTokens, p.chunk);
   if (ns == 1) return;  // written directly by the split kernel
   // the partials are written by the split kernel launched just before
   asm volatile("griddepcontrol.wait;" ::: "memory");

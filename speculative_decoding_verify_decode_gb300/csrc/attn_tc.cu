@@ -47,7 +47,7 @@
 namespace sdv {
 namespace {
 
-constexpr int kT = 128;                 // tokens per tile
+constexpr int kT = kTileTokens;         // tokens per tile
 constexpr int kGroupB = 4096;           // 8 token rows x 4 dim blocks x 128 B
 constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 256 dims
 constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
@@ -55,6 +55,7 @@ constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 1
 constexpr int kThreads = 224;
 constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
+constexpr float kNoMax = -1.0e30f;      // the running maximum before any visible score
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 
 // The V tile moves in two 64-token halves (pages 0-3 and 4-7, each 32 KB
@@ -73,9 +74,11 @@ struct Small {
   float red[4][kCols];
   float lsum[4][kCols];   // per softmax warp: column sums of P over its 32 token rows
   int outrow[kCols];    // output row (node row * 24 + head) of each query column (-1: padding)
+  int lo_col[kCols];    // sliding window: oldest context position each query column sees
   uint64_t bar[NUM_BARS];
   unsigned long long anc[kMaxNodes];    // bit r of anc[n]: draft node r is node n or one of its ancestors
   int par[kMaxNodes];
+  int depth[kMaxNodes];   // draft CTA with a window: depth of each node
   // Row copies of the staging pass: source row (null: zeros), byte offset of
   // the row's chunk 0 in the dynamic shared memory, and its 64-dim block stride.
   const __nv_bfloat16* rsrc[kMaxStageRows];
@@ -87,7 +90,7 @@ struct Small {
 };
 static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &&
                   offsetof(Small, red) % 16 == 0 && offsetof(Small, lsum) % 16 == 0 &&
-                  offsetof(Small, outrow) % 16 == 0,
+                  offsetof(Small, outrow) % 16 == 0 && offsetof(Small, lo_col) % 16 == 0,
               "per-column arrays must be 16-byte aligned");
 static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + sizeof(Small) <= 232448,
@@ -291,7 +294,9 @@ __device__ __forceinline__ float transpose_max32(float (&v)[32], int lane) {
   return v[0];
 }
 
-template <int NQ>
+// WIN: compiled with the sliding-window paths (band masks, depths); the
+// instances without them serve full attention.
+template <int NQ, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
@@ -333,8 +338,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // [(s - 1) * chunk, s * chunk).  The producers fetch their first tile's page
   // ids beside the context length (any entry of the table row is in bounds).
   const bool has_draft = (s == 0);
+  const int W = WIN ? p.window : 0;
   int page0 = -1;
-  if ((warp == kWarpK || warp == kWarpV) && lane < 8 && !has_draft) {
+  if ((warp == kWarpK || warp == kWarpV) && lane < 8 && !has_draft && W <= 0) {
     const long long idx = (((long long)(s - 1) * p.chunk) >> 4) + lane;
     if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
   }
@@ -343,9 +349,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (s == 0 && c == 0 && g == 0 && tid == 0) report(p.dev_status, SD_DEV_BAD_CTX);
     L = L < 0 ? 0 : p.max_pages * kPage;
   }
-  const int nsplit = active_splits(L, p.chunk);
+  // with a window the splits cover the tiles from the root's oldest visible position on
+  const int base = window_base(L, W, kT);
+  const int nsplit = active_splits(L, W, kT, p.chunk);
   if (s >= nsplit) return;
-  const int ctx_begin = has_draft ? 0 : (s - 1) * p.chunk;
+  const int ctx_begin = has_draft ? 0 : base + (s - 1) * p.chunk;
+  if (W > 0 && (warp == kWarpK || warp == kWarpV) && lane < 8 && !has_draft) {
+    const long long idx = (ctx_begin >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
   const int ctx_end = has_draft ? 0 : min(L, ctx_begin + p.chunk);
   const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
   const int head0 = g * kGroup + c * hpc;
@@ -364,11 +376,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int q = tid; q < kCols; q += kThreads) {
-    sm->m[q] = q < NQ ? -INFINITY : 0.f;
+    // Running maxima start finite and far below any score: a column that has
+    // seen no visible key yet (possible with a window) then gives masked scores
+    // exp2(-inf - m) = 0, not NaN, and its first visible score takes the
+    // rescaling path like any score more than 2^8 above the maximum.
+    sm->m[q] = q < NQ ? kNoMax : 0.f;
     sm->alpha[q] = 1.f;
     sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
   }
-  if (has_draft && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];   // one load each; the walk below is in shared memory
+  // one load each; the walks below are in shared memory (every CTA needs the depths with a window)
+  if ((has_draft || W > 0) && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];
   __syncthreads();  // mbarriers and per-column arrays ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -494,6 +511,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   {
     const int ct = tid - 32;
     if (!has_draft) stage_operands(ct, 5 * 32, false);
+    if (W > 0) {
+      // oldest visible context position of each query column: L + depth(node) - W + 1
+      // (padding columns take the root's; an invalid parent chain stops the walk)
+      const float inv_hpc = 1.0f / (float)hpc;
+      for (int q = ct; q < kCols; q += 5 * 32) {
+        int d = 0;
+        if (q < rows) {
+          for (int u = __float2int_rz(((float)q + 0.5f) * inv_hpc); u > 0 && d < kMaxNodes; ++d) {
+            const int pu = sm->par[u];
+            if (pu < 0 || pu >= u) break;
+            u = pu;
+          }
+        }
+        sm->lo_col[q] = L + d - W + 1;
+      }
+    }
     if (warp == kWarpMma) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -644,19 +677,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (has_draft) {
       if (row < n_nodes) {
         unsigned long long a = 1ull << row;
+        int d = 0;
         bool ok = row == 0 ? sm->par[0] == -1 : true;
-        for (int u = row; ok && u > 0;) {
+        for (int u = row; ok && u > 0; ++d) {
           const int pu = sm->par[u];
           ok = pu >= 0 && pu < u;
           if (ok) a |= 1ull << pu;
           u = pu;
         }
-        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << row; }
+        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << row; d = 0; }
         sm->anc[row] = a;
+        sm->depth[row] = d;
       }
       masks_ok = group_sync();
       if (row < n_nodes) {
-        for (int n = row; n < n_nodes; ++n) my_desc |= ((sm->anc[n] >> row) & 1ull) << n;
+        // with a window, a descendant n more than W - 1 levels below does not see `row`
+        const int dr = sm->depth[row];
+        for (int n = row; n < n_nodes; ++n)
+          if (W <= 0 || sm->depth[n] - dr < W) my_desc |= ((sm->anc[n] >> row) & 1ull) << n;
       }
     }
     for (int i = 0; i < n_tiles && masks_ok; ++i) {
@@ -676,6 +714,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       for (int gq = 0; gq < NG; ++gq) {
         const int ncol = min(32, NQ - gq * 32);
         vis[gq] = (!draft_tile && row < valid) ? (ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u)) : 0u;
+      }
+      if (!draft_tile && W > 0 && t0 < L - W + 1 + kMaxNodes) {
+        // tiles inside the window's band: column q sees token t0 + row from lo_col[q] on
+        const int tpos = t0 + row;
+#pragma unroll
+        for (int gq = 0; gq < NG; ++gq) {
+          uint32_t bits = 0u;
+#pragma unroll 1
+          for (int e = 0; e < 32; ++e) bits |= (tpos >= sm->lo_col[gq * 32 + e] ? 1u : 0u) << e;
+          vis[gq] &= bits;
+        }
       }
       if (draft_tile) {
         unsigned long long d = my_desc;
@@ -886,7 +935,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int q = col + e;
-          const float inv = __fdividef(1.0f, l[e]);
+          const float inv = l[e] > 0.f ? __fdividef(1.0f, l[e]) : 0.f;   // no visible key in this split: 0
           stage[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
           stage[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
         }
@@ -967,11 +1016,11 @@ bool cache_map(CUtensorMap* map, const void* cache, int pool_pages) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NQ>
+template <int NQ, bool WIN>
 cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, const BatchDesc& bd,
                       int hpc, int hparts, cudaStream_t st) {
   const size_t smem = tc_smem_bytes(NQ);
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NQ, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits * kHkv * hparts, bd.batch);
@@ -983,7 +1032,7 @@ cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnPa
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ>, mk, mv, p, bd, hpc, hparts);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ, WIN>, mk, mv, p, bd, hpc, hparts);
 }
 
 }  // namespace
@@ -1013,13 +1062,19 @@ cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_
   if (!cache_map(&mk, p.k_cache, p.num_pool_pages) || !cache_map(&mv, p.v_cache, p.num_pool_pages))
     return cudaErrorInvalidValue;
   const TcPlan pl = tc_plan(bd.max_nodes);
+  const bool win = p.window > 0;
   cudaError_t e;
   switch (pl.nq) {
-    case 32: e = launch_nq<32>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
-    case 48: e = launch_nq<48>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
-    case 64: e = launch_nq<64>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
-    case 80: e = launch_nq<80>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
-    case 96: e = launch_nq<96>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
+    case 32: e = win ? launch_nq<32, true>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                     : launch_nq<32, false>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
+    case 48: e = win ? launch_nq<48, true>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                     : launch_nq<48, false>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
+    case 64: e = win ? launch_nq<64, true>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                     : launch_nq<64, false>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
+    case 80: e = win ? launch_nq<80, true>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                     : launch_nq<80, false>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
+    case 96: e = win ? launch_nq<96, true>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                     : launch_nq<96, false>(mk, mv, p, bd, pl.hpc, pl.hparts, st); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess || p.num_splits == 1) return e;

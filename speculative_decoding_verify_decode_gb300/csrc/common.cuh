@@ -15,6 +15,7 @@ constexpr int kHkv = 4;          // KV heads
 constexpr int kGroup = kHq / kHkv;
 constexpr int kDim = 256;        // head_dim
 constexpr int kPage = 16;        // tokens per KV page
+constexpr int kTileTokens = 128; // context tokens per attention tile (the MMA's M)
 constexpr int kMaxNodes = SD_MAX_NODES;
 constexpr int kMaxBatch = SD_MAX_BATCH;
 constexpr int kMaxLayers = SD_MAX_LAYERS;
@@ -50,6 +51,7 @@ struct AttnParams {
   int num_pool_pages;
   int chunk;             // context tokens per split (multiple of the kernel's tile)
   int num_splits;
+  int window;            // sliding window (0: the whole context)
 };
 
 __device__ __forceinline__ void report(int* status, int bits) {
@@ -68,11 +70,22 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// First context position a sequence's splits cover: 0 for full attention;
+// with a window W, the root's oldest visible position L - W + 1, rounded down
+// to a multiple of `tile` (the splits start on tile boundaries).
+__host__ __device__ __forceinline__ int window_base(int L, int window, int tile) {
+  if (window <= 0) return 0;
+  const int first = L - window + 1;
+  return first <= 0 ? 0 : first / tile * tile;
+}
+
 // Number of active splits of a sequence with context length L: split 0
 // attends to the draft block alone and splits 1.. to consecutive chunks of
-// `chunk` context tokens, so a sequence without context has one split.
-__host__ __device__ __forceinline__ int active_splits(int L, int chunk) {
-  return 1 + (L > 0 ? (L + chunk - 1) / chunk : 0);
+// `chunk` context tokens from window_base on, so a sequence without
+// (visible) context has one split.
+__host__ __device__ __forceinline__ int active_splits(int L, int window, int tile, int chunk) {
+  const int span = L - window_base(L, window, tile);
+  return 1 + (span > 0 ? (span + chunk - 1) / chunk : 0);
 }
 
 }  // namespace sdv

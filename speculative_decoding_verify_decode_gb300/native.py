@@ -35,7 +35,8 @@ class SdShape(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("max_pages_per_seq", ctypes.c_int), ("num_pool_pages", ctypes.c_int),
-                ("num_splits", ctypes.c_int)]
+                ("num_splits", ctypes.c_int),
+                ("window", ctypes.c_int)]
 
 
 class SdError(RuntimeError):
@@ -113,10 +114,12 @@ def _indptr(q_indptr) -> ctypes.Array:
 class Shape:
     """An sd_shape with its host q_indptr kept alive."""
 
-    def __init__(self, q_indptr, max_pages_per_seq: int, num_pool_pages: int, num_splits: int = 0):
+    def __init__(self, q_indptr, max_pages_per_seq: int, num_pool_pages: int, num_splits: int = 0,
+                 window: int = 0):
         self.indptr = _indptr(q_indptr)
         self.c = SdShape(len(self.indptr) - 1, ctypes.cast(self.indptr, ctypes.POINTER(ctypes.c_int)),
-                         24, 4, 256, 16, int(max_pages_per_seq), int(num_pool_pages), int(num_splits))
+                         24, 4, 256, 16, int(max_pages_per_seq), int(num_pool_pages), int(num_splits),
+                         int(window))
 
     @property
     def ref(self):

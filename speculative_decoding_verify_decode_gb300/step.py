@@ -18,14 +18,15 @@ class VerifyStep:
     """Buffers and calls for one verify step of a fixed batch shape."""
 
     def __init__(self, q_indptr, max_pages_per_seq: int, num_pool_pages: int, num_layers: int, vocab: int,
-                 device="cuda", num_splits: int = 0, max_path: int | None = None, want_lse: bool = False):
+                 device="cuda", num_splits: int = 0, max_path: int | None = None, want_lse: bool = False,
+                 window: int = 0):
         self.q_indptr = np.asarray(q_indptr, dtype=np.int32)
         self.batch = len(self.q_indptr) - 1
         self.total = int(self.q_indptr[-1])
         self.num_layers = int(num_layers)
         self.vocab = int(vocab)
         self.device = torch.device(device)
-        self.shape = native.Shape(self.q_indptr, max_pages_per_seq, num_pool_pages, num_splits)
+        self.shape = native.Shape(self.q_indptr, max_pages_per_seq, num_pool_pages, num_splits, window)
         self.max_path = int(max_path or int(np.diff(self.q_indptr).max()))
         dev = self.device
         ws = native.sd_verify_attn_workspace_size(self.shape)

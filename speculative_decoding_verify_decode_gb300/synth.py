@@ -75,6 +75,7 @@ class Workload:
     k_cache: list = field(default_factory=list)  # per layer bf16 [P, 4, 16, 256]
     v_cache: list = field(default_factory=list)
     logits: torch.Tensor | None = None           # fp32 [sum N, V]
+    window: int = 0                              # sliding window (0: the whole context)
 
     @property
     def total_nodes(self) -> int:
@@ -101,6 +102,9 @@ CONFIGS = {
                                 vocab=151936, p=(0.5, 0.9), seed=3, table="permuted"),
     "ddtree22_ctx128k": dict(batch=1, layers=16, ctx=131072, tree="ddtree", budget=22,
                              vocab=151936, p=0.85, seed=5, table="permuted"),
+    # sliding-window verify: attention over the most recent 2,048 positions of a long context
+    "chain8_ctx32k_win2048": dict(batch=1, layers=16, ctx=32768, tree="chain", K=8, vocab=151936,
+                                  p=0.8, seed=12, table="permuted", window=2048),
 }
 
 
@@ -291,5 +295,6 @@ def make_workload(name: str, device="cpu", layers: int | None = None, qkv_scale:
     w = make_structure(batch, ctx, parents_list, cfg["seed"], cfg["vocab"], p_list,
                        planted_list, table=cfg["table"], rescue=rescue, rng=rng)
     w.name = name
+    w.window = int(cfg.get("window", 0))
     nl = cfg["layers"] if layers is None else layers
     return fill_tensors(w, nl, cfg["seed"], device=device, qkv_scale=qkv_scale, logits=logits)

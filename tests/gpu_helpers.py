@@ -57,16 +57,18 @@ def check_attention(out: torch.Tensor, ref: np.ndarray, lse: torch.Tensor | None
     return out
 
 
-def oracle_attention(w, layer: int, samples=None):
+def oracle_attention(w, layer: int, samples=None, window: int | None = None):
+    win = getattr(w, "window", 0) if window is None else window
     return oracle.verify_attention(f32(w.q[layer]), f32(w.k_cache[layer]), f32(w.v_cache[layer]),
                                    f32(w.k_new[layer]), f32(w.v_new[layer]), w.page_table, w.ctx_lens,
-                                   w.q_indptr, w.parents, samples=samples)
+                                   w.q_indptr, w.parents, samples=samples, window=win or None)
 
 
-def gpu_attention(w, layer: int, num_splits: int = 0, want_lse: bool = True):
+def gpu_attention(w, layer: int, num_splits: int = 0, want_lse: bool = True, window: int | None = None):
     d = device_inputs(w)
+    win = getattr(w, "window", 0) if window is None else window
     st = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, 1, max(w.vocab, 1), num_splits=num_splits,
-                    want_lse=want_lse)
+                    want_lse=want_lse, window=win)
     st.attention(0, w.q[layer], w.k_cache[layer], w.v_cache[layer], w.k_new[layer], w.v_new[layer],
                  d["page_table"], d["ctx_lens"], d["parents"])
     torch.cuda.synchronize()
