@@ -162,6 +162,33 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 # ---------------------------------------------------------------- GPU arm
 
+def time_ddtree_build(dev, stream, batch: int, budget: int, positions: int = 16, vocab: int = 151936,
+                      topk: int = 8, reps: int = 50) -> dict:
+    """The draft-tree construction that precedes a tree verify step, timed on its own: top-8 of
+    every draft position's logits, then the best-first tree of `budget` nodes (one draft block of
+    16 positions per sequence, as on the DDTree page)."""
+    logits = torch.from_numpy(synth.draft_logits(batch, positions, vocab, seed=17)).to(dev)
+    roots = torch.zeros(batch, dtype=torch.int32, device=dev)
+    par = torch.empty((batch, 1 + budget), dtype=torch.int32, device=dev)
+    tok = torch.empty_like(par)
+    ws = torch.empty(native.sd_ddtree_workspace_size(batch, positions, vocab, topk), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(3):
+        native.sd_ddtree_build(logits, topk, budget, roots, par, tok, None, ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        native.sd_ddtree_build(logits, topk, budget, roots, par, tok, None, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    gbs = batch * positions * vocab * 4 / (us * 1e-6) / 1e9
+    peak, _ = peaks()
+    return {"us": us, "logits_gbs": gbs, "frac": gbs / peak, "launches": 2,
+            "shape": {"batch": batch, "positions": positions, "vocab": vocab, "topk": topk, "budget": budget}}
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -279,6 +306,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk.summary(),
     }
+    if args.config.startswith("ddtree"):
+        line["ddtree_build"] = time_ddtree_build(dev, stream, w.batch, w.total_nodes // w.batch - 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.config, reps=1)
     return line

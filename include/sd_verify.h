@@ -222,6 +222,47 @@ sd_status sd_kv_commit(const sd_shape* shape, int num_layers, void* const* k_cac
                        const int* ctx_lens, int* new_ctx_lens, const int* accept_len,
                        const int* path, int max_path, int* dev_status, void* stream);
 
+/*
+ * sd_ddtree_build — the draft tree the verify step checks, built from the
+ * draft model's logits for a block of `positions` positions
+ * («如何在单张 RTX 3090 上让 Qwen3.5-27B token 生成速度提升 6 倍», 从自回归到 DDTree:
+ * a draft block of 16 positions becomes a token tree of `budget` nodes;
+ * 关键突破: per-position top-K (32 -> 8), chain pre-seed).
+ *
+ * Per position d, the candidates are the topk tokens with the largest draft
+ * logits (ties: the smaller token id first), scored by log-probability
+ * logit - log(sum(exp(logits of the position))).  A node at depth d >= 1 holds
+ * a candidate of position d - 1 and scores the sum of the log-probabilities on
+ * its root path.  The rank-0 chain is inserted first, down to depth
+ * min(positions, budget); then, until the tree has 1 + budget nodes, the best
+ * of the candidates "first child (rank 0, one position deeper) of an inserted
+ * node" and "next sibling (rank + 1, same parent) of an inserted node" is
+ * inserted (ties: the candidate created first).  Node 0 is the root with
+ * token root_tokens[b]; nodes are numbered in insertion order, so
+ * parents[j] < j and the outputs feed sd_verify_attn / sd_accept directly
+ * (q_indptr = b * (1 + budget)).
+ *
+ *   batch                      1..SD_MAX_BATCH
+ *   positions                  1..SD_MAX_NODES
+ *   vocab                      >= topk
+ *   topk                       1..8
+ *   budget                     1..SD_MAX_NODES - 1 (non-root nodes)
+ *   draft_logits               fp32 [batch][positions][vocab]
+ *   root_tokens                int32 [batch]
+ *   parents, tokens            int32 [batch][1 + budget], written; entries past the available
+ *                              candidates are -1
+ *   scores                     fp32 [batch][1 + budget] or NULL (path log-probabilities)
+ *   workspace                  >= sd_ddtree_workspace_size bytes, 16-byte aligned
+ * Errors: bad sizes or null pointers -> SD_ERR_INVALID_ARG / SD_ERR_UNSUPPORTED
+ * before any launch; NaN logits -> SD_DEV_NAN_LOGITS in *dev_status (the tree
+ * is then unspecified).
+ */
+size_t sd_ddtree_workspace_size(int batch, int positions, int vocab, int topk);
+sd_status sd_ddtree_build(int batch, int positions, int vocab, int topk, int budget,
+                          const float* draft_logits, const int* root_tokens, int* parents, int* tokens,
+                          float* scores, void* workspace, size_t ws_bytes, int* dev_status,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

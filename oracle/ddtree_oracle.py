@@ -63,8 +63,8 @@ def build_tree(cand_tokens, cand_logprobs, budget: int, root_token: int):
     """Best-first tree of 1 + budget nodes over the candidates (see the module notes).
 
     Returns (parents [n], tokens [n], scores [n], margin): `margin` is the smallest
-    score gap between the candidate inserted and the best one left behind, over
-    all best-first decisions (inf when no choice was contested).
+    score gap between the candidate inserted and the best lower-scored one left
+    behind, over all best-first decisions (inf when no choice was contested).
     """
     positions, k = cand_tokens.shape
     parents, tokens, scores = [-1], [int(root_token)], [0.0]
@@ -93,8 +93,9 @@ def build_tree(cand_tokens, cand_logprobs, budget: int, root_token: int):
     margin = float("inf")
     while len(parents) < 1 + budget and heap:
         neg, _, par, dep, rk = heapq.heappop(heap)
-        if heap:
-            margin = min(margin, heap[0][0] - neg)       # gap to the best candidate left behind
+        lower = [h[0] for h in heap if h[0] > neg]      # candidates left behind with a lower score
+        if lower:                                       # (equal scores are ordered by creation on
+            margin = min(margin, min(lower) - neg)       # any hardware, so they are not a contest)
         node = len(parents)
         parents.append(par)
         tokens.append(int(cand_tokens[dep - 1, rk]))

@@ -232,4 +232,49 @@ sd_status sd_kv_commit(const sd_shape* shape, int num_layers, void* const* k_cac
   return cuda_status(launch_commit(p, bd, static_cast<cudaStream_t>(stream)));
 }
 
+size_t sd_ddtree_workspace_size(int batch, int positions, int vocab, int topk) {
+  if (batch < 1 || batch > kMaxBatch || positions < 1 || positions > kMaxNodes || topk < 1 ||
+      topk > kDdTopKMax || vocab < topk)
+    return 0;
+  const size_t rows = (size_t)batch * positions;
+  const size_t chunks = ((size_t)vocab + kDdChunk - 1) / kDdChunk;
+  return align_up(rows * chunks * kDdTopKMax * sizeof(float)) + align_up(rows * chunks * kDdTopKMax * sizeof(int)) +
+         align_up(rows * chunks * 2 * sizeof(float));
+}
+
+sd_status sd_ddtree_build(int batch, int positions, int vocab, int topk, int budget, const float* draft_logits,
+                          const int* root_tokens, int* parents, int* tokens, float* scores, void* workspace,
+                          size_t ws_bytes, int* dev_status, void* stream) {
+  if (batch < 1 || positions < 1 || topk < 1 || budget < 1 || vocab < 1) return SD_ERR_INVALID_ARG;
+  if (batch > kMaxBatch || positions > kMaxNodes || topk > kDdTopKMax || budget > kMaxNodes - 1)
+    return SD_ERR_UNSUPPORTED;
+  if (vocab < topk || !draft_logits || !root_tokens || !parents || !tokens) return SD_ERR_INVALID_ARG;
+  const size_t need = sd_ddtree_workspace_size(batch, positions, vocab, topk);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return SD_ERR_WORKSPACE;
+  if ((vocab % 4 == 0) && !aligned16(draft_logits)) return SD_ERR_INVALID_ARG;
+  const int chunks = (vocab + kDdChunk - 1) / kDdChunk;
+  if (ddtree_smem_bytes(chunks) > 200 * 1024) return SD_ERR_UNSUPPORTED;
+  DdtreeParams p;
+  std::memset(&p, 0, sizeof(p));
+  const size_t rows = (size_t)batch * positions;
+  char* ws = static_cast<char*>(workspace);
+  p.logits = draft_logits;
+  p.root_tokens = root_tokens;
+  p.parents = parents;
+  p.tokens = tokens;
+  p.scores = scores;
+  p.dev_status = dev_status;
+  p.part_v = reinterpret_cast<float*>(ws);
+  p.part_i = reinterpret_cast<int*>(ws + align_up(rows * chunks * kDdTopKMax * sizeof(float)));
+  p.part_ms = reinterpret_cast<float*>(ws + align_up(rows * chunks * kDdTopKMax * sizeof(float)) +
+                                       align_up(rows * chunks * kDdTopKMax * sizeof(int)));
+  p.batch = batch;
+  p.positions = positions;
+  p.vocab = vocab;
+  p.topk = topk;
+  p.budget = budget;
+  p.chunks = chunks;
+  return cuda_status(launch_ddtree(p, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -57,4 +57,22 @@ struct CommitParams {
 };
 cudaError_t launch_commit(const CommitParams& p, const BatchDesc& bd, cudaStream_t st);
 
+// Draft-tree construction: per-position top-K of the draft logits, then a best-first tree.
+constexpr int kDdTopKMax = 8;      // candidates per position
+constexpr int kDdChunk = 4096;     // logits per chunk of the top-K pass (16 per thread)
+struct DdtreeParams {
+  const float* logits;       // [batch][positions][vocab]
+  const int* root_tokens;    // [batch]
+  int* parents;              // [batch][1 + budget]
+  int* tokens;               // [batch][1 + budget]
+  float* scores;             // [batch][1 + budget], nullable
+  int* dev_status;           // nullable
+  float* part_v;             // [batch * positions][chunks][8] chunk top-8 values
+  int* part_i;               // [batch * positions][chunks][8] and their token ids
+  float* part_ms;            // [batch * positions][chunks][2] (max, sum of exp(x - max))
+  int batch, positions, vocab, topk, budget, chunks;
+};
+size_t ddtree_smem_bytes(int chunks);
+cudaError_t launch_ddtree(const DdtreeParams& p, cudaStream_t st);
+
 }  // namespace sdv

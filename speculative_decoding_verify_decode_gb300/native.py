@@ -75,6 +75,10 @@ def load() -> ctypes.CDLL:
     lib.sd_kv_commit.restype = ctypes.c_int
     pp = ctypes.POINTER(ctypes.c_void_p)
     lib.sd_kv_commit.argtypes = [shp, ctypes.c_int, pp, pp, pp, pp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.sd_ddtree_workspace_size.restype = sz
+    lib.sd_ddtree_workspace_size.argtypes = [ctypes.c_int] * 4
+    lib.sd_ddtree_build.restype = ctypes.c_int
+    lib.sd_ddtree_build.argtypes = [ctypes.c_int] * 5 + [vp, vp, vp, vp, vp, vp, sz, vp, vp]
     _lib = lib
     return lib
 
@@ -186,3 +190,18 @@ def sd_kv_commit(shape: Shape, k_cache_layers, v_cache_layers, k_new_layers, v_n
                                _ptr(ctx_lens), _ptr(new_ctx_lens), _ptr(accept_len), _ptr(path),
                                int(max_path), _ptr(dev_status), _stream(stream)),
            "sd_kv_commit")
+
+
+def sd_ddtree_workspace_size(batch: int, positions: int, vocab: int, topk: int) -> int:
+    return int(load().sd_ddtree_workspace_size(int(batch), int(positions), int(vocab), int(topk)))
+
+
+def sd_ddtree_build(draft_logits, topk: int, budget: int, root_tokens, parents, tokens, scores=None,
+                    workspace=None, dev_status=None, stream=None) -> None:
+    """draft_logits fp32 [batch, positions, vocab]; parents/tokens int32 [batch, 1 + budget]."""
+    batch, positions, vocab = (int(x) for x in draft_logits.shape)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().sd_ddtree_build(batch, positions, vocab, int(topk), int(budget), _ptr(draft_logits),
+                                  _ptr(root_tokens), _ptr(parents), _ptr(tokens), _ptr(scores), _ptr(workspace),
+                                  ws_bytes, _ptr(dev_status), _stream(stream)),
+           "sd_ddtree_build")

@@ -298,3 +298,17 @@ def make_workload(name: str, device="cpu", layers: int | None = None, qkv_scale:
     w.window = int(cfg.get("window", 0))
     nl = cfg["layers"] if layers is None else layers
     return fill_tensors(w, nl, cfg["seed"], device=device, qkv_scale=qkv_scale, logits=logits)
+
+
+def draft_logits(batch: int, positions: int, vocab: int, seed: int, scale: float = 2.0,
+                 ties: bool = False) -> np.ndarray:
+    """Seeded draft-model logits [batch, positions, vocab] (fp32) for the draft-tree builder.
+
+    N(0, scale) entries; with ``ties`` every value is rounded to a coarse grid
+    (multiples of 0.25), so that equal logits occur, also across 4096-entry chunks.
+    """
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0.0, scale, size=(batch, positions, vocab)).astype(np.float32)
+    if ties:
+        x = np.round(x * 4.0) / 4.0
+    return x

@@ -111,3 +111,25 @@ def test_commit_host_checks(lib):
     assert call(native.MAX_LAYERS + 1) == native.SD_ERR_UNSUPPORTED
     assert call(2, k=nul) == native.SD_ERR_INVALID_ARG
     assert call(2, new=FAKE, ctx=FAKE) == native.SD_ERR_INVALID_ARG   # new_ctx_lens aliases ctx_lens
+
+
+def test_ddtree_host_checks(lib):
+    ws = FAKE
+    call = lambda b, p, v, k, n, ws_bytes=1 << 30, logits=FAKE: lib.sd_ddtree_build(
+        b, p, v, k, n, logits, FAKE, FAKE, FAKE, None, ws, ws_bytes, None, None)
+    assert call(1, 16, 151936, 9, 22) == native.SD_ERR_UNSUPPORTED        # topk > 8
+    assert call(1, 65, 151936, 8, 22) == native.SD_ERR_UNSUPPORTED        # positions > 64
+    assert call(1, 16, 151936, 8, 64) == native.SD_ERR_UNSUPPORTED        # 1 + budget > 64
+    assert call(0, 16, 151936, 8, 22) == native.SD_ERR_INVALID_ARG
+    assert call(1, 16, 4, 8, 22) == native.SD_ERR_INVALID_ARG             # vocab < topk
+    assert call(1, 16, 151936, 8, 22, logits=None) == native.SD_ERR_INVALID_ARG
+    assert call(1, 16, 151936, 8, 22, ws_bytes=16) == native.SD_ERR_WORKSPACE
+    assert lib.sd_ddtree_workspace_size(1, 16, 151936, 8) > 0
+    assert lib.sd_ddtree_workspace_size(1, 16, 151936, 9) == 0
+
+
+def test_negative_window_is_rejected(lib):
+    s = _shape()
+    s.c.window = -1
+    assert _attn(lib, s) == native.SD_ERR_INVALID_ARG
+    assert lib.sd_verify_attn_workspace_size(s.ref) == 0
