@@ -10,14 +10,15 @@
 // Kernel 1 scans fixed 4096-logit chunks of every (sequence, position) row
 // with 128-bit loads; each thread keeps its 16 values' top 8 in registers
 // (largest value first, equal values: smaller token id first), the warps merge
-// theirs by 8 rounds of shuffle argmax, and the chunk's top 8 is written with
+// theirs by 8 rounds of redux.sync argmax, and the chunk's top 8 is written with
 // the chunk's (max, sum of exp(x - max)) for the log-sum-exp.
 // Kernel 2 runs one block per sequence: sixteen warps merge the chunk lists of
 // the positions (all of a position's records in one round of loads) and form
 // log-probabilities (logit - log-sum-exp); one warp then inserts the rank-0
 // chain up to depth min(positions, budget) and adds the best remaining
-// candidate (two redux.sync maxima over an order-preserving score key and the
-// inverted creation number) until the tree holds 1 + budget nodes.  The
+// candidate (kept in registers across the warp; two redux.sync maxima over an
+// order-preserving score key and the inverted creation number) until the tree
+// holds 1 + budget nodes.  The
 // candidates are, for every inserted node, its first child (rank 0, one
 // position deeper) and its next sibling (rank + 1, same parent); score = the
 // summed log-probabilities of the root path; ties go to the candidate created
@@ -54,25 +55,35 @@ __device__ __forceinline__ void insert_sorted(float (&tv)[kK], int (&ti)[kK], fl
   }
 }
 
+// Order-preserving 32-bit key of a float (larger float -> larger key; -0 and +0
+// must be folded by the caller, NaN excluded).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Warp-wide argmax of (value, id) pairs with ties to the smaller id: two
+// redux.sync, the largest value key, then the smallest id among the lanes holding it.
+__device__ __forceinline__ void warp_best(float v, int i, float& bv, int& bi) {
+  const uint32_t k = order_key(v + 0.0f);                 // -0 -> +0
+  const uint32_t bk = __reduce_max_sync(0xffffffffu, k);
+  bi = (int)__reduce_min_sync(0xffffffffu, k == bk ? (uint32_t)i : 0xffffffffu);
+  bv = key_value(bk);
+}
+
 // Warp-wide: the best of the lanes' list heads; the winning lane drops its head.
 // Returns the winner (same on every lane).
 __device__ __forceinline__ void warp_pop_best(float (&tv)[kK], int (&ti)[kK], float& wv, int& wi) {
-  float bv = tv[0];
-  int bi = ti[0];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-    if (before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-  }
-  if (tv[0] == bv && ti[0] == bi) {   // ids are distinct, so exactly one lane (or none for padding) matches
+  warp_best(tv[0], ti[0], wv, wi);
+  if ((tv[0] + 0.0f) == wv && ti[0] == wi) {   // ids are distinct: one lane matches (padding lanes may too)
 #pragma unroll
     for (int j = 0; j < kK - 1; ++j) { tv[j] = tv[j + 1]; ti[j] = ti[j + 1]; }
     tv[kK - 1] = -INFINITY;
     ti[kK - 1] = INT_MAX;
   }
-  wv = bv;
-  wi = bi;
 }
 
 // (max, sum of exp(x - max)) pairs: combine b into a.
@@ -184,12 +195,6 @@ __global__ void __launch_bounds__(kThreads1) topk_chunk_kernel(const DdtreeParam
   }
 }
 
-// Order-preserving 32-bit key of a float (larger float -> larger key).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 __global__ void __launch_bounds__(kThreads2) ddtree_build_kernel(const DdtreeParams p) {
   extern __shared__ __align__(16) uint8_t dyn[];
   const int b = blockIdx.x;
@@ -244,12 +249,7 @@ __global__ void __launch_bounds__(kThreads2) ddtree_build_kernel(const DdtreePar
         const int i = wi[r];
         if (before(pv, pi, v, i) && before(v, i, bv, bi)) { bv = v; bi = i; }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
+      warp_best(bv, bi, bv, bi);
       if (lane == 0) { s_tok[d][k] = bi; s_lp[d][k] = bv - lse; }
       pv = bv;
       pi = bi;
@@ -258,23 +258,26 @@ __global__ void __launch_bounds__(kThreads2) ddtree_build_kernel(const DdtreePar
   }
   __syncthreads();
   if (warp != 0) return;
-  // ---- best-first insertion (warp 0; every lane tracks the same counters)
+  // ---- best-first insertion (warp 0).  Candidate number c lives in lane c % 32,
+  // register slot c / 32: (score, parent's score, creation number, parent | depth << 8 | rank << 16).
   __shared__ int n_par[kMaxNodes], n_tok[kMaxNodes];
   __shared__ float n_sc[kMaxNodes];
-  __shared__ float k_sc[kMaxCand];
-  __shared__ int k_seq[kMaxCand], k_par[kMaxCand], k_dep[kMaxCand], k_rank[kMaxCand];
+  constexpr int kSlots = (kMaxCand + 31) / 32;
+  float c_sc[kSlots], c_psc[kSlots];
+  int c_seq[kSlots], c_info[kSlots];
+#pragma unroll
+  for (int k = 0; k < kSlots; ++k) { c_sc[k] = -INFINITY; c_psc[k] = 0.f; c_seq[k] = -1; c_info[k] = 0; }
   const int P = p.positions, K = p.topk, budget = p.budget;
   const int chain = min(P, budget);
   int ncand = 0;
-  // append candidate (parent, depth, rank) as number ncand; lane 0 writes, all lanes count
   auto push = [&](int par, int dep, int rank, float par_score) {
     if (dep > P || rank >= K || ncand >= kMaxCand) return;
-    if (lane == 0) {
-      k_sc[ncand] = par_score + s_lp[dep - 1][rank];
-      k_seq[ncand] = ncand;               // creation order = slot number
-      k_par[ncand] = par;
-      k_dep[ncand] = dep;
-      k_rank[ncand] = rank;
+    const float sc = par_score + s_lp[dep - 1][rank];
+    const int slot = ncand >> 5;
+    if (lane == (ncand & 31)) {
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k)
+        if (k == slot) { c_sc[k] = sc; c_psc[k] = par_score; c_seq[k] = ncand; c_info[k] = par | (dep << 8) | (rank << 16); }
     }
     ++ncand;
   };
@@ -301,38 +304,45 @@ __global__ void __launch_bounds__(kThreads2) ddtree_build_kernel(const DdtreePar
     }
     push(chain, chain + 1, 0, chain_sc);    // the chain's continuation
   }
-  __syncwarp();
   int nodes = 1 + chain;
   while (nodes < 1 + budget) {
-    // this lane's best live candidate, as (order key of the score, inverted creation number)
+    // this lane's best live candidate: largest score, then smallest creation number
     uint32_t k1 = 0u, k2 = 0u;
-    int mine = -1;
-    for (int c = lane; c < ncand; c += 32) {
-      if (k_seq[c] < 0) continue;             // taken
-      const uint32_t a1 = order_key(k_sc[c]), a2 = ~(uint32_t)k_seq[c];
-      if (mine < 0 || a1 > k1 || (a1 == k1 && a2 > k2)) { k1 = a1; k2 = a2; mine = c; }
+    int bk = -1;
+    float bsc = 0.f, bpsc = 0.f;
+    int binfo = 0;
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      if (c_seq[k] < 0) continue;
+      const uint32_t a1 = order_key(c_sc[k] + 0.0f), a2 = ~(uint32_t)c_seq[k];
+      if (bk < 0 || a1 > k1 || (a1 == k1 && a2 > k2)) {
+        k1 = a1; k2 = a2; bk = k; bsc = c_sc[k]; bpsc = c_psc[k]; binfo = c_info[k];
+      }
     }
-    const unsigned live = __ballot_sync(0xffffffffu, mine >= 0);
-    if (live == 0u) break;                    // no candidate left
-    const uint32_t best1 = __reduce_max_sync(0xffffffffu, mine >= 0 ? k1 : 0u);
-    const uint32_t best2 = __reduce_max_sync(0xffffffffu, (mine >= 0 && k1 == best1) ? k2 : 0u);
-    const unsigned owner = __ballot_sync(0xffffffffu, mine >= 0 && k1 == best1 && k2 == best2);
-    const int bc = __shfl_sync(0xffffffffu, mine, __ffs(owner) - 1);
-    const int par = k_par[bc], dep = k_dep[bc], rank = k_rank[bc];
-    const float sc = k_sc[bc];
+    if (__ballot_sync(0xffffffffu, bk >= 0) == 0u) break;   // no candidate left
+    const uint32_t best1 = __reduce_max_sync(0xffffffffu, bk >= 0 ? k1 : 0u);
+    const uint32_t best2 = __reduce_max_sync(0xffffffffu, (bk >= 0 && k1 == best1) ? k2 : 0u);
+    const bool mine = bk >= 0 && k1 == best1 && k2 == best2;
+    const int owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    const float sc = __shfl_sync(0xffffffffu, bsc, owner);
+    const float psc = __shfl_sync(0xffffffffu, bpsc, owner);
+    const int info = __shfl_sync(0xffffffffu, binfo, owner);
+    if (mine) {
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k) if (k == bk) c_seq[k] = -1;   // taken
+    }
+    const int par = info & 0xff, dep = (info >> 8) & 0xff, rank = info >> 16;
     const int node = nodes;
-    __syncwarp();
     if (lane == 0) {
       n_par[node] = par;
       n_tok[node] = s_tok[dep - 1][rank];
       n_sc[node] = sc;
-      k_seq[bc] = -1;
     }
     push(node, dep + 1, 0, sc);               // its first child
-    push(par, dep, rank + 1, n_sc[par]);      // its next sibling
+    push(par, dep, rank + 1, psc);            // its next sibling
     ++nodes;
-    __syncwarp();
   }
+  __syncwarp();
   const int out0 = b * (1 + budget);
   for (int j = lane; j < 1 + budget; j += 32) {
     const bool live = j < nodes;
