@@ -2,6 +2,7 @@
 // checks, workspace layout, split-KV sizing, and the kernel launches.  Nothing
 // here allocates device memory or synchronises; every launch goes on the
 // caller's stream.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -96,6 +97,108 @@ sd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SD_OK : SD_ERR_
 // The kernels move bf16 rows with 16-byte vector accesses.
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A per-tensor scale of an e4m3 cache: positive, finite, with a finite fp32 reciprocal.
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && std::isfinite(1.0f / s); }
+
+// sd_verify_attn and sd_verify_attn_fp8: checks, split plan, parameter block, launch.
+sd_status verify_attn(const sd_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                      const void* k_new, const void* v_new, const int* page_table, const int* ctx_lens,
+                      const int* parents, void* out, float* lse, void* workspace, size_t ws_bytes, int* dev_status,
+                      void* stream, bool fp8, float k_scale, float v_scale) {
+  BatchDesc bd;
+  sd_status st = check_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (!q || !k_cache || !v_cache || !k_new || !v_new || !page_table || !ctx_lens || !parents || !out)
+    return SD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
+    return SD_ERR_INVALID_ARG;
+  if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return SD_ERR_INVALID_ARG;
+  const SplitPlan pl = plan_splits(shape, bd);
+  const size_t need = attn_workspace(pl, bd);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SD_ERR_WORKSPACE;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  if (fp8) {
+    p.k_cache8 = static_cast<const uint8_t*>(k_cache);
+    p.v_cache8 = static_cast<const uint8_t*>(v_cache);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+  } else {
+    p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+    p.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  }
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.page_table = page_table;
+  p.ctx_lens = ctx_lens;
+  p.parents = parents;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.dev_status = dev_status;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pool_pages = shape->num_pool_pages;
+  p.chunk = pl.chunk;
+  p.num_splits = pl.nsplit;
+  p.window = shape->window;
+  if (need > 0) {
+    const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
+    p.o_part = static_cast<__nv_bfloat16*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(__nv_bfloat16)));
+  }
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return cuda_status(fp8 ? launch_attn_tc8(p, bd, cs) : launch_attn_tc(p, bd, cs));
+}
+
+// sd_kv_commit and sd_kv_commit_fp8.
+sd_status kv_commit(const sd_shape* shape, int num_layers, void* const* k_cache_layers, void* const* v_cache_layers,
+                    const float* k_scales, const float* v_scales, const void* const* k_new_layers,
+                    const void* const* v_new_layers, const int* page_table, const int* ctx_lens, int* new_ctx_lens,
+                    const int* accept_len, const int* path, int max_path, int* dev_status, void* stream, bool fp8) {
+  BatchDesc bd;
+  sd_status st = check_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (num_layers < 1) return SD_ERR_INVALID_ARG;
+  if (num_layers > kMaxLayers) return SD_ERR_UNSUPPORTED;
+  if (!k_cache_layers || !v_cache_layers || !k_new_layers || !v_new_layers || !page_table || !ctx_lens ||
+      !accept_len || !path || max_path < 1)
+    return SD_ERR_INVALID_ARG;
+  if (fp8 && (!k_scales || !v_scales)) return SD_ERR_INVALID_ARG;
+  if (new_ctx_lens != nullptr && new_ctx_lens == ctx_lens) return SD_ERR_INVALID_ARG;
+  CommitParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_cache_layers[l] || !v_cache_layers[l] || !k_new_layers[l] || !v_new_layers[l])
+      return SD_ERR_INVALID_ARG;
+    if (!aligned16(k_cache_layers[l]) || !aligned16(v_cache_layers[l]) || !aligned16(k_new_layers[l]) ||
+        !aligned16(v_new_layers[l]))
+      return SD_ERR_INVALID_ARG;
+    if (fp8) {
+      if (!scale_ok(k_scales[l]) || !scale_ok(v_scales[l])) return SD_ERR_INVALID_ARG;
+      p.k_inv[l] = 1.0f / k_scales[l];
+      p.v_inv[l] = 1.0f / v_scales[l];
+    }
+    p.k_cache[l] = k_cache_layers[l];
+    p.v_cache[l] = v_cache_layers[l];
+    p.k_new[l] = k_new_layers[l];
+    p.v_new[l] = v_new_layers[l];
+  }
+  p.fp8 = fp8 ? 1 : 0;
+  p.page_table = page_table;
+  p.ctx_lens = ctx_lens;
+  p.new_ctx_lens = new_ctx_lens;
+  p.accept_len = accept_len;
+  p.path = path;
+  p.dev_status = dev_status;
+  p.max_path = max_path;
+  p.max_pages = shape->max_pages_per_seq;
+  p.num_pool_pages = shape->num_pool_pages;
+  p.num_layers = num_layers;
+  return cuda_status(launch_commit(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -121,42 +224,16 @@ sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cac
                          const void* k_new, const void* v_new, const int* page_table, const int* ctx_lens,
                          const int* parents, void* out, float* lse, void* workspace, size_t ws_bytes,
                          int* dev_status, void* stream) {
-  BatchDesc bd;
-  sd_status st = check_shape(shape, &bd);
-  if (st != SD_OK) return st;
-  if (!q || !k_cache || !v_cache || !k_new || !v_new || !page_table || !ctx_lens || !parents || !out)
-    return SD_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
-      !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
-    return SD_ERR_INVALID_ARG;
-  const SplitPlan pl = plan_splits(shape, bd);
-  const size_t need = attn_workspace(pl, bd);
-  if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SD_ERR_WORKSPACE;
+  return verify_attn(shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, out, lse, workspace,
+                     ws_bytes, dev_status, stream, false, 1.f, 1.f);
+}
 
-  AttnParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  p.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
-  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  p.page_table = page_table;
-  p.ctx_lens = ctx_lens;
-  p.parents = parents;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lse = lse;
-  p.dev_status = dev_status;
-  p.max_pages = shape->max_pages_per_seq;
-  p.num_pool_pages = shape->num_pool_pages;
-  p.chunk = pl.chunk;
-  p.num_splits = pl.nsplit;
-  p.window = shape->window;
-  if (need > 0) {
-    const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
-    p.o_part = static_cast<__nv_bfloat16*>(workspace);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(__nv_bfloat16)));
-  }
-  return cuda_status(launch_attn_tc(p, bd, static_cast<cudaStream_t>(stream)));
+sd_status sd_verify_attn_fp8(const sd_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                             float k_scale, float v_scale, const void* k_new, const void* v_new,
+                             const int* page_table, const int* ctx_lens, const int* parents, void* out, float* lse,
+                             void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+  return verify_attn(shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, out, lse, workspace,
+                     ws_bytes, dev_status, stream, true, k_scale, v_scale);
 }
 
 size_t sd_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {
@@ -197,39 +274,18 @@ sd_status sd_kv_commit(const sd_shape* shape, int num_layers, void* const* k_cac
                        const void* const* v_new_layers, const int* page_table, const int* ctx_lens,
                        int* new_ctx_lens, const int* accept_len, const int* path, int max_path,
                        int* dev_status, void* stream) {
-  BatchDesc bd;
-  sd_status st = check_shape(shape, &bd);
-  if (st != SD_OK) return st;
-  if (num_layers < 1) return SD_ERR_INVALID_ARG;
-  if (num_layers > kMaxLayers) return SD_ERR_UNSUPPORTED;
-  if (!k_cache_layers || !v_cache_layers || !k_new_layers || !v_new_layers || !page_table || !ctx_lens ||
-      !accept_len || !path || max_path < 1)
-    return SD_ERR_INVALID_ARG;
-  if (new_ctx_lens != nullptr && new_ctx_lens == ctx_lens) return SD_ERR_INVALID_ARG;
-  CommitParams p;
-  std::memset(&p, 0, sizeof(p));
-  for (int l = 0; l < num_layers; ++l) {
-    if (!k_cache_layers[l] || !v_cache_layers[l] || !k_new_layers[l] || !v_new_layers[l])
-      return SD_ERR_INVALID_ARG;
-    if (!aligned16(k_cache_layers[l]) || !aligned16(v_cache_layers[l]) || !aligned16(k_new_layers[l]) ||
-        !aligned16(v_new_layers[l]))
-      return SD_ERR_INVALID_ARG;
-    p.k_cache[l] = k_cache_layers[l];
-    p.v_cache[l] = v_cache_layers[l];
-    p.k_new[l] = k_new_layers[l];
-    p.v_new[l] = v_new_layers[l];
-  }
-  p.page_table = page_table;
-  p.ctx_lens = ctx_lens;
-  p.new_ctx_lens = new_ctx_lens;
-  p.accept_len = accept_len;
-  p.path = path;
-  p.dev_status = dev_status;
-  p.max_path = max_path;
-  p.max_pages = shape->max_pages_per_seq;
-  p.num_pool_pages = shape->num_pool_pages;
-  p.num_layers = num_layers;
-  return cuda_status(launch_commit(p, bd, static_cast<cudaStream_t>(stream)));
+  return kv_commit(shape, num_layers, k_cache_layers, v_cache_layers, nullptr, nullptr, k_new_layers, v_new_layers,
+                   page_table, ctx_lens, new_ctx_lens, accept_len, path, max_path, dev_status, stream, false);
+}
+
+sd_status sd_kv_commit_fp8(const sd_shape* shape, int num_layers, void* const* k_cache_layers,
+                           void* const* v_cache_layers, const float* k_scales, const float* v_scales,
+                           const void* const* k_new_layers, const void* const* v_new_layers,
+                           const int* page_table, const int* ctx_lens, int* new_ctx_lens, const int* accept_len,
+                           const int* path, int max_path, int* dev_status, void* stream) {
+  return kv_commit(shape, num_layers, k_cache_layers, v_cache_layers, k_scales, v_scales, k_new_layers,
+                   v_new_layers, page_table, ctx_lens, new_ctx_lens, accept_len, path, max_path, dev_status, stream,
+                   true);
 }
 
 size_t sd_ddtree_workspace_size(int batch, int positions, int vocab, int topk) {

@@ -1,0 +1,1166 @@
+// Split-KV verify attention on the 5th-generation tensor cores (tcgen05,
+// accumulators in tensor memory) with TMA-staged K/V pages.
+//
+// What it computes is the same as the tree/causal-masked grouped-query
+// attention of the verify step: for sequence b, draft node j and query head
+// h, softmax attention (scale 1/16) of q[j][h] over every context token of KV
+// head h/6 plus the draft nodes on j's root path.  Sources, by page title:
+// «如何在单张 RTX 3090 上让 Qwen3.5-27B token 生成速度提升 6 倍» (为什么我们要做这个测试:
+// 24 Q / 4 KV heads, head dim 256; 关键突破: the tree mask follows each node's
+// parent chain) and «Qwen3.8-27B投机解码实测：从14到159 tok/s的性能断点地图» (§2, §4:
+// 16-token pages from one pool; §5.3: bottom-right causal mask of a chain).
+//
+// Layout of the work.  A CTA owns (split s, KV head g, head part c, sequence
+// b): hpc query heads of group g (6, 3, 2 or 1, so that hpc * N <= 96)
+// times the sequence's N draft nodes form NQ (multiple of 16) query columns.
+// Tokens are the MMA's M dimension ("swap-AB"), so a 128-token K/V tile
+// serves every query column at once:
+//   S^T[128 tok][NQ]  = K_tile[128 tok][256] . Q^T                (K-major A and B)
+//   O^T[256 dim][NQ] += V_tile^T[256][128 tok] . P^T[128 tok][NQ]  (MN-major A and B)
+//   l[NQ]            += 1^T . P^T                                  (column sums of P)
+// S^T (double-buffered), O^T and l live in tensor memory (5 * NQ <= 480 of
+// the 512 columns).  The column sums are taken by the tensor core from the
+// same bf16 P^T the PV product uses.  When a sequence needs several CTAs for
+// its query heads (hpc < 6), the CTAs of one split are adjacent in launch
+// order and read the same pages while they are still in L2.
+//
+// Operand tiles (Q^T, K, V) are "block-major": four 64-dim blocks, each
+// holding every row of the tile at 128 B with the 128-byte swizzle, so the
+// UMMA descriptors step 1 KB between 8-row groups.  A TMA box of 16 rows x 64
+// dims (one page of one KV head, one block) writes 2 KB of a block; a
+// 128-token tile takes 32 boxes.
+//
+// Warp roles (224 threads): warp 0 streams K tiles and warp 6 V tiles with
+// TMA; warp 1 allocates tensor memory and one lane issues every tcgen05.mma,
+// taking QK of tile i and PV of tile i-1 in whichever order their inputs
+// arrive; warps 2-5 (one per tensor-memory lane quarter, thread = token row)
+// run the online softmax: masking, a running per-column maximum that is only
+// raised (and O^T, l rescaled) when a score exceeds it by more than 2^8,
+// exp2, and the bf16 P^T tile.  Every wait on an mbarrier is bounded; on
+// expiry the kernel reports SD_DEV_TIMEOUT and winds down.
+//
+// Quantised cache (KV8).  The context K/V pages hold e4m3 codes with one
+// scale per tensor (K, V) of the layer; the key and value a code stands for is
+// decode(code) * scale (the quantised KV cache of «如何在单张 RTX 3090 上让
+// Qwen3.5-27B token 生成速度提升 6 倍», 24 GB 显存上的 128K 上下文, here in e4m3).
+// Four converter warps (0 and 7 for K, 6 and 8 for V) take the producers'
+// place: each loads its pages of the next tile into registers with 16-byte
+// loads as soon as it has stored the current one (the register file is a
+// second tile buffer), waits for the tile buffer to be released, widens the
+// codes to f16 (every e4m3 value is exact in f16) in the same group-major
+// swizzled layout, and signals the MMA.  Q^T, P^T and the draft block are f16
+// too, so the products are kind::f16 with f16 operands.  The K scale joins
+// the softmax multiplier and the V scale the epilogue's normalisation; the
+// draft block (not yet committed, so not quantised) has scale 1.
+#pragma once
+
+#include <cstddef>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sdv {
+namespace {
+
+constexpr int kT = kTileTokens;         // tokens per tile
+constexpr int kGroupB = 4096;           // 8 token rows x 4 dim blocks x 128 B
+constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 256 dims
+constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
+constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
+constexpr int kThreads = 224;
+constexpr int kThreads8 = 288;          // the quantised-cache instances: two more converter warps
+constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
+constexpr int kWarpK2 = 7, kWarpV2 = 8;  // second K / V converter warp (quantised cache)
+constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
+constexpr float kNoMax = -1.0e30f;      // the running maximum before any visible score
+constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
+
+// The V tile moves in two 64-token halves (pages 0-3 and 4-7, each 32 KB
+// contiguous), so that the first half of the next tile loads while the PV
+// product still reads the second half of this one.
+// A quantised K tile is also filled and released in two halves of the head
+// dimension (K_FULL / K_EMPTY: dims 0-127, K_FULL1 / K_EMPTY1: dims 128-255).
+enum Bar { K_FULL, K_EMPTY, V_FULL0, V_FULL1, V_EMPTY0, V_EMPTY1, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE,
+           GROUP, K_FULL1, K_EMPTY1, NUM_BARS };
+
+constexpr int kCols = 128;   // per-column arrays padded to whole 32-column groups
+constexpr int kMaxStageRows = kTcMaxNQ + 2 * kMaxNodes;   // Q^T rows + the draft block's K and V rows
+
+// Per-column arrays first: each is read with 16-byte vector loads.
+struct Small {
+  float m[kCols];
+  float alpha[kCols];
+  float red[4][kCols];
+  float lsum[4][kCols];   // per softmax warp: column sums of P over its 32 token rows
+  int outrow[kCols];    // output row (node row * 24 + head) of each query column (-1: padding)
+  int lo_col[kCols];    // sliding window: oldest context position each query column sees
+  uint64_t bar[NUM_BARS];
+  unsigned long long anc[kMaxNodes];    // bit r of anc[n]: draft node r is node n or one of its ancestors
+  int par[kMaxNodes];
+  int depth[kMaxNodes];   // draft CTA with a window: depth of each node
+  // Row copies of the staging pass: source row (null: zeros), byte offset of
+  // the row's chunk 0 in the dynamic shared memory, and its 64-dim block stride.
+  const __nv_bfloat16* rsrc[kMaxStageRows];
+  uint32_t rdst[kMaxStageRows];
+  uint32_t rblk[kMaxStageRows];
+  int flag[2][4];
+  uint32_t tmem;
+  int abort;
+};
+static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &&
+                  offsetof(Small, red) % 16 == 0 && offsetof(Small, lsum) % 16 == 0 &&
+                  offsetof(Small, outrow) % 16 == 0 && offsetof(Small, lo_col) % 16 == 0,
+              "per-column arrays must be 16-byte aligned");
+static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + sizeof(Small) <= 232448,
+              "the widest tile configuration must fit in 227 KB of shared memory");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------ mbarrier / TMA
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+// Test a phase; the waiting thread is suspended in hardware (up to about
+// 10 ms, or until the phase completes) instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(10000000u)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false (and the CTA's abort flag set) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Small* sm, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
+      sm->abort = 1;
+      report(status, SD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded spin on a phase (no suspension): the softmax warps have nothing
+// else to do while they wait, and a spin sees the phase flip soonest.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, Small* sm, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
+      sm->abort = 1;
+      report(status, SD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// One page of one KV head (8 KB) into shared memory: the 4-D box of the
+// cache map at outer coordinate w, x = y = z = 0.
+__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------ tcgen05
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
+// stride byte offsets (16-byte units), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: bf16 x bf16 (or f16 x f16) -> f32, M x N, operand majors.
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n, int a_mn, int b_mn, bool bf16 = true) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+
+// Byte offset of 16-byte chunk c (0..31) of token row r in a group-major
+// K/V tile: 8-row group r/8 (4 KB), 64-dim block c/8 (1 KB), row r%8,
+// swizzled chunk (c%8) ^ (r%8).  A page's 16 rows are 8 contiguous KB.
+__device__ __forceinline__ uint32_t kv_off(int r, int c) {
+  return (uint32_t)((r >> 3) * kGroupB + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// Byte offset of 16-byte chunk cc (0..7) of token row r in the P^T tile
+// (MN-major: 64-column atoms of 128 rows x 128 B, 128-byte swizzle).
+__device__ __forceinline__ uint32_t p_off(int r, int cc) {
+  return (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
+}
+
+// Copy `nrows` rows of 256 bf16 into rows r0.. of a group-major K/V tile
+// (row r's source is src_of(r), or zeros when that is null).  `nthreads`
+// threads starting at `t` share the work; each keeps 8 independent 16-byte
+// loads in flight.
+template <typename SrcFn>
+__device__ __forceinline__ void stage_rows(uint8_t* base, int r0, int nrows, SrcFn src_of, int t, int nthreads) {
+  constexpr int U = 8;
+  const int tasks = nrows * 32;
+  for (int t0 = t; t0 < tasks; t0 += nthreads * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int task = t0 + u * nthreads;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (task < tasks) {
+        const __nv_bfloat16* src = src_of(task >> 5);
+        if (src != nullptr) v[u] = __ldg(reinterpret_cast<const uint4*>(src) + (task & 31));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int task = t0 + u * nthreads;
+      if (task < tasks) *reinterpret_cast<uint4*>(base + kv_off(r0 + (task >> 5), task & 31)) = v[u];
+    }
+  }
+}
+
+// ------------------------------------------------------------ quantised cache
+
+// Eight bf16 (one 16-byte chunk) as eight f16, rounded to nearest.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
+  auto one = [](uint32_t w) -> uint32_t {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  return make_uint4(one(v.x), one(v.y), one(v.z), one(v.w));
+}
+// Two e4m3 codes (low byte first) as two f16 (exact: e4m3 is a subset of f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(two & 0xffffu)));
+  return r;
+}
+// 16 bytes of a streamed cache page; no L1 allocation (each page is read once per CTA).
+__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+// 16 e4m3 codes (dims 16c .. 16c + 15 of token row r) widened into the two
+// f16 chunks 2c and 2c + 1 of a group-major K/V tile.  Lanes whose chunk has
+// bit 2 set store the odd chunk first, so that each group of 8 lanes (one row,
+// two 64-dim blocks) covers all 32 banks in both stores.
+__device__ __forceinline__ void store_widened(uint8_t* tile, int r, int c, const uint4 v) {
+  const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                              e4m3x2_to_f16x2(v.y >> 16));
+  const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                              e4m3x2_to_f16x2(v.w >> 16));
+  const bool odd_first = (c & 4) != 0;
+  const uint32_t a_lo = kv_off(r, 2 * c), a_hi = kv_off(r, 2 * c + 1);
+  *reinterpret_cast<uint4*>(tile + (odd_first ? a_hi : a_lo)) = odd_first ? hi : lo;
+  *reinterpret_cast<uint4*>(tile + (odd_first ? a_lo : a_hi)) = odd_first ? lo : hi;
+}
+
+// Bits [start, start + len) of a 32-bit word (clipped to the word).
+__device__ __forceinline__ uint32_t bit_range(int start, int len) {
+  const int a = max(start, 0), e = min(start + len, 32);
+  if (e <= a) return 0u;
+  const uint32_t upto = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+  return upto & ~((1u << a) - 1u);
+}
+
+// Element g of a small per-thread array, by a select chain rather than a
+// dynamically indexed (local-memory) access.
+template <int N>
+__device__ __forceinline__ uint32_t vis_of(const uint32_t (&a)[N], int g) {
+  uint32_t r = a[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) r = (g == k) ? a[k] : r;
+  return r;
+}
+
+// Reduce 32 values per lane across the warp so that lane L ends with the
+// maximum over all lanes of value L (transpose-reduce, 31 shuffles).
+__device__ __forceinline__ float transpose_max32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
+    }
+  }
+  return v[0];
+}
+
+// WIN: compiled with the sliding-window paths (band masks, depths); the
+// instances without them serve full attention.
+// KV8: the quantised-cache instance (e4m3 pages, f16 operands, converter warps).
+template <int NQ, bool WIN, bool KV8>
+__global__ void __launch_bounds__(KV8 ? kThreads8 : kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
+  constexpr int NG = (NQ + 31) / 32;          // 32-column groups
+  constexpr int NATOM = (NQ + 63) / 64;       // 64-column atoms of the P^T tile
+  constexpr int kQB = NQ * 512;               // Q^T tile: 4 blocks of NQ rows x 128 B
+  constexpr uint32_t kColS0 = 0, kColO = 2 * NQ;   // tensor-memory columns
+  static_assert(4 * NQ <= 512, "tensor memory holds 2 S^T and 2 O^T halves");
+  // The kernel declares no static shared memory, so the dynamic window starts
+  // at a 1024-byte boundary (required by the 128-byte swizzle atoms); indexing
+  // it directly keeps every access a shared-space one.
+  extern __shared__ __align__(1024) uint8_t dyn_smem[];
+  uint8_t* sQ = dyn_smem;
+  uint8_t* sK = sQ + kQB;
+  uint8_t* sV = sK + kTileB;
+  uint8_t* sP = sV + kTileB;
+  Small* sm = reinterpret_cast<Small*>(sP + NATOM * kAtomB);
+
+  constexpr int NT = KV8 ? kThreads8 : kThreads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // warps that fill the K/V tiles: TMA producers, or converters for a quantised cache
+  const bool producer = warp == kWarpK || warp == kWarpV || (KV8 && (warp == kWarpK2 || warp == kWarpV2));
+  const int bid = blockIdx.x;
+  const int c = bid % hparts;
+  const int g = (bid / hparts) % kHkv;
+  const int s = bid / (hparts * kHkv);
+  const int b = blockIdx.y;
+  const int q0 = bd.q_indptr[b];
+  const int n_nodes = bd.q_indptr[b + 1] - q0;
+  const int rows = hpc * n_nodes;
+  if (c * hpc >= kGroup) return;
+  // Launched as a programmatic dependent: wait for the previous kernel in the
+  // stream before touching global memory, then let the merge kernel's blocks
+  // be scheduled (they wait for this grid to finish before reading).
+  // the producers fetch their TMA descriptor while the rest of the prologue runs
+  if (!KV8 && (warp == kWarpK || warp == kWarpV) && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpK ? &tm_k : &tm_v))
+                 : "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Split 0 attends to the draft block alone; split s >= 1 to context tokens
+  // [(s - 1) * chunk, s * chunk).  The producers fetch their first tile's page
+  // ids beside the context length (any entry of the table row is in bounds).
+  const bool has_draft = (s == 0);
+  const int W = WIN ? p.window : 0;
+  int page0 = -1;
+  if (producer && lane < 8 && !has_draft && W <= 0) {
+    const long long idx = (((long long)(s - 1) * p.chunk) >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
+  int L = p.ctx_lens[b];
+  if (L < 0 || L > p.max_pages * kPage) {
+    if (s == 0 && c == 0 && g == 0 && tid == 0) report(p.dev_status, SD_DEV_BAD_CTX);
+    L = L < 0 ? 0 : p.max_pages * kPage;
+  }
+  // with a window the splits cover the tiles from the root's oldest visible position on
+  const int base = window_base(L, W, kT);
+  const int nsplit = active_splits(L, W, kT, p.chunk);
+  if (s >= nsplit) return;
+  const int ctx_begin = has_draft ? 0 : base + (s - 1) * p.chunk;
+  if (W > 0 && producer && lane < 8 && !has_draft) {
+    const long long idx = (ctx_begin >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
+  const int ctx_end = has_draft ? 0 : min(L, ctx_begin + p.chunk);
+  const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
+  const int head0 = g * kGroup + c * hpc;
+  if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
+    if (threadIdx.x == 0) report(p.dev_status, SD_DEV_TIMEOUT);
+    return;
+  }
+
+  // ---------------------------------------------------------------- prologue
+  if (tid == 0) {
+    for (int i = 0; i < NUM_BARS; ++i) {
+      // a quantised tile is complete when both of its converter warps have arrived
+      const bool conv = KV8 && (i == K_FULL || i == K_FULL1 || i == V_FULL0 || i == V_FULL1);
+      const uint32_t cnt = (i == S_FREE0 || i == S_FREE1 || i == P_FULL || i == GROUP) ? 4u : conv ? 2u : 1u;
+      mbar_init(smem_u32(&sm->bar[i]), cnt);
+    }
+    sm->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int q = tid; q < kCols; q += NT) {
+    // Running maxima start finite and far below any score: a column that has
+    // seen no visible key yet (possible with a window) then gives masked scores
+    // exp2(-inf - m) = 0, not NaN, and its first visible score takes the
+    // rescaling path like any score more than 2^8 above the maximum.
+    sm->m[q] = q < NQ ? kNoMax : 0.f;
+    sm->alpha[q] = 1.f;
+    sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
+  }
+  // one load each; the walks below are in shared memory (every CTA needs the depths with a window)
+  if ((has_draft || W > 0) && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];
+  __syncthreads();  // mbarriers and per-column arrays ready
+  const uint32_t bars = smem_u32(&sm->bar[0]);
+  auto bar = [&](int i) { return bars + 8u * i; };
+
+  // Staging of the operands that do not come by TMA, by `nthr` threads
+  // (index t): Q^T (K-major, block-major; column q = node * hpc +
+  // head-in-part, the hpc heads of a node being adjacent rows of q; zeros past
+  // `rows`) and, in the draft CTA, the draft block as the K and V tiles
+  // (group-major; node t = token row t).  A row table (source, destination,
+  // block stride) is built first, then one pass of 16-byte copies with up to
+  // 16 loads in flight per thread; the last round repeats the final chunk
+  // instead of branching, so the unrolled copies stay independent.
+  auto stage_operands = [&](const int t, const int nthr, const bool all_warps) {
+    const float inv_hpc = 1.0f / (float)hpc;
+    const int n_stage = NQ + (has_draft ? 2 * n_nodes : 0);
+    for (int r = t; r < n_stage; r += nthr) {
+      const __nv_bfloat16* src;
+      uint32_t dst, blk;
+      if (r < NQ) {
+        const int node = __float2int_rz(((float)r + 0.5f) * inv_hpc);   // r / hpc, exact for r < 2^20
+        src = r < rows ? p.q + ((size_t)(q0 + node) * kHq + head0 + r - node * hpc) * kDim : nullptr;
+        dst = (uint32_t)(sQ - dyn_smem) + r * 128;
+        blk = NQ * 128;
+      } else {
+        const bool is_v = r >= NQ + n_nodes;
+        const int tok = r - NQ - (is_v ? n_nodes : 0);
+        src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + tok) * kHkv + g) * kDim;
+        dst = (uint32_t)((is_v ? sV : sK) - dyn_smem) + (tok >> 3) * kGroupB + (tok & 7) * 128;
+        blk = 1024;
+      }
+      sm->rsrc[r] = src;
+      sm->rdst[r] = dst;
+      sm->rblk[r] = blk;
+    }
+    if (all_warps) __syncthreads();
+    else asm volatile("bar.sync 3, 160;" ::: "memory");   // the five compute warps
+    constexpr int U = 16;
+    const int tasks = n_stage * 32;
+    for (int t0 = t; t0 - t < tasks; t0 += nthr * U) {
+      uint4 v[U];
+      uint32_t d[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int task = min(t0 + u * nthr, tasks - 1);
+        const int r = task >> 5, c = task & 31;
+        const __nv_bfloat16* src = sm->rsrc[r];
+        const uint32_t off = sm->rdst[r];
+        v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0, 0, 0, 0);
+        d[u] = off + (c >> 3) * sm->rblk[r] + (((c & 7) ^ ((off >> 7) & 7)) << 4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dyn_smem + d[u]) = KV8 ? bf16x8_to_f16x8(v[u]) : v[u];
+    }
+  };
+  if (has_draft) {
+    // The draft CTA has no TMA work: all warps stage its operands.  V
+    // rows from the block's end to the next 16-row boundary are zeroed (the
+    // draft tile's PV product stops there; P^T is 0 on them, but 0 times stale
+    // shared memory could be NaN).  S^T rows past the block are masked.
+    stage_operands(tid, NT, true);
+    const int v_end = (n_nodes + 15) & ~15;
+    for (int i = tid; i < (v_end - n_nodes) * 32; i += NT)
+      *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();   // plain stores above, read by the tensor core
+    __syncthreads();
+  }
+
+  if (KV8 && producer) {
+    // ------------------------------------------------------------ converters (quantised cache)
+    // Each tile is converted in two halves, each held in registers (16 loads
+    // of 16 bytes per lane) while the half's buffer may still be in use:
+    //   K half h: dims 128h .. 128h + 127 of every token row (QK steps 8h ..
+    //     8h + 7); warp wi takes pages wi + 2j (j < 4); lane l: slot l/8 + 4u,
+    //     16-byte chunk l%8 + 8h, so 8 lanes read one 128-byte half row;
+    //   V half h: pages 4h .. 4h + 3 (the 64-token halves the PV product
+    //     consumes); warp wi takes pages 4h + wi + 2j (j < 2); lane l: slot
+    //     l/16 + 2u, chunk l%16, so 16 lanes read one 256-byte row.
+    const bool is_k = warp == kWarpK || warp == kWarpK2;
+    const int wi = (warp == kWarpK || warp == kWarpV) ? 0 : 1;
+    uint8_t* dst = is_k ? sK : sV;
+    const uint8_t* cache = is_k ? p.k_cache8 : p.v_cache8;
+    const int n_ctx = has_draft ? 0 : n_tiles;
+    int page_next = page0;
+    auto publish = [&](uint32_t full) {
+      fence_async_smem();   // plain stores, read by the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full);
+    };
+    bool ok = true;
+    for (int i = 0; i < n_ctx && ok; ++i) {
+      const int t0 = ctx_begin + i * kT;
+      const int valid = min(kT, ctx_end - t0);
+      int page = (lane < 8 && lane * kPage < valid) ? page_next : -1;
+      if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
+        page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
+      if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
+        report(p.dev_status, SD_DEV_BAD_PAGE);
+        page = -1;
+      }
+      const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
+      for (int h = 0; h < 2 && ok; ++h) {
+        uint4 v[16];
+        int row[16], chunk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int pi = is_k ? wi + 2 * (k >> 2) : 4 * h + wi + 2 * (k >> 3);
+          const int slot = is_k ? (lane >> 3) + 4 * (k & 3) : (lane >> 4) + 2 * (k & 7);
+          chunk[k] = is_k ? (lane & 7) + 8 * h : (lane & 15);
+          row[k] = pi * kPage + slot;
+          const int pg = __shfl_sync(0xffffffffu, page, pi);
+          const bool in = pg >= 0 && row[k] < valid;
+          v[k] = in ? ld_stream16(cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim + chunk[k] * 16)
+                    : make_uint4(0, 0, 0, 0);
+        }
+        const uint32_t empty = bar(is_k ? (h == 0 ? K_EMPTY : K_EMPTY1) : (h == 0 ? V_EMPTY0 : V_EMPTY1));
+        if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) store_widened(dst, row[k], chunk[k], v[k]);
+        publish(bar(is_k ? (h == 0 ? K_FULL : K_FULL1) : (h == 0 ? V_FULL0 : V_FULL1)));
+      }
+      if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
+    }
+  } else if (!KV8 && producer) {
+    // ------------------------------------------------------------ TMA producers (K or V)
+    const bool is_k = warp == kWarpK;
+    uint8_t* dst = is_k ? sK : sV;
+    const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    const int nparts = is_k ? 1 : 2;           // K: one 8-page part; V: two 4-page halves
+    const int ppp = 8 / nparts;                 // pages per part
+    const int n_ctx = has_draft ? 0 : n_tiles;   // the draft CTA stages its block without TMA
+    int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
+    for (int i = 0; i < n_ctx; ++i) {
+      const int t0 = ctx_begin + i * kT;
+      const int valid = min(kT, ctx_end - t0);
+      int page = (lane < 8 && lane * kPage < valid) ? page_next : -1;
+      if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
+        page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
+      if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
+        report(p.dev_status, SD_DEV_BAD_PAGE);
+        page = -1;
+      }
+      // a page goes by TMA when it is in range and all 16 of its tokens are valid
+      const bool page_full = page >= 0 && (lane + 1) * kPage <= valid;
+      const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page_full);
+      const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
+      bool ok = true;
+      for (int part = 0; part < nparts && ok; ++part) {
+        const uint32_t full = bar(is_k ? K_FULL : V_FULL0 + part), empty = bar(is_k ? K_EMPTY : V_EMPTY0 + part);
+        const uint32_t part_mask = ((1u << ppp) - 1u) << (part * ppp);
+        if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        // pages that are partial, missing or out of range: plain copies, zero past the context
+        for (int pi = part * ppp; pi < (part + 1) * ppp; ++pi) {
+          if (tma_mask & (1u << pi)) continue;
+          const int pg = __shfl_sync(0xffffffffu, page, pi);
+          stage_rows(dst, pi * kPage, kPage, [&](int slot) -> const __nv_bfloat16* {
+            return (pg >= 0 && pi * kPage + slot < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim
+                                                          : nullptr;
+          }, lane, 32);
+        }
+        if ((tma_mask & part_mask) != part_mask) fence_async_smem();   // plain copies above: visible to the MMA
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(tma_mask & part_mask) * kPageB);
+        __syncwarp();
+        // lane l: page l of the tile, one 8 KB box
+        if (((part_mask & tma_mask) >> lane) & 1u)
+          tma_load_page(smem_u32(dst + lane * kPageB), map, (page * kHkv + g) * 2, full);
+      }
+      if (!ok) break;
+      if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
+    }
+  } else {
+  // ---------------------------------------------------------------- compute warps (1-5)
+  // While the producers fetch the first tiles, these five warps stage Q^T
+  // (and split 0's draft block, tile 0) and allocate tensor memory.
+  {
+    const int ct = tid - 32;
+    if (!has_draft) stage_operands(ct, 5 * 32, false);
+    if (W > 0) {
+      // oldest visible context position of each query column: L + depth(node) - W + 1
+      // (padding columns take the root's; an invalid parent chain stops the walk)
+      const float inv_hpc = 1.0f / (float)hpc;
+      for (int q = ct; q < kCols; q += 5 * 32) {
+        int d = 0;
+        if (q < rows) {
+          for (int u = __float2int_rz(((float)q + 0.5f) * inv_hpc); u > 0 && d < kMaxNodes; ++d) {
+            const int pu = sm->par[u];
+            if (pu < 0 || pu >= u) break;
+            u = pu;
+          }
+        }
+        sm->lo_col[q] = L + d - W + 1;
+      }
+    }
+    if (warp == kWarpMma) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_fence_before();
+    asm volatile("bar.sync 1, 160;" ::: "memory");   // the five compute warps, all arrive unconditionally
+    tc_fence_after();
+  }
+  const uint32_t tmem = sm->tmem;
+  if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = f16_idesc(128, NQ, 0, 0, !KV8);
+      constexpr uint32_t kIdescPV = f16_idesc(128, NQ, 1, 1, !KV8);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
+      int kf = 0, pf = 0, vf0 = 0, vf1 = 0;
+      int pv_half = 0;   // the PV product of a context tile runs in two 64-token halves
+      int sfree[2] = {0, 0};
+      int qk_next = 0, pv_next = 0;
+      long long idle_since = clock64();
+      while (pv_next < n_tiles) {
+        bool progressed = false;
+        // QK of the next tile: K tile landed, S^T buffer released by the softmax
+        if (qk_next < n_tiles && qk_next <= pv_next + 1) {
+          const int i = qk_next, sb = i & 1;
+          // (a quantised K tile arrives in two halves of the head dimension)
+          const bool k_ok = (has_draft && i == 0) ||
+                            (mbar_test(bar(K_FULL), kf & 1) && (!KV8 || mbar_test(bar(K_FULL1), kf & 1)));
+          const bool s_ok = i < 2 || mbar_test(bar(S_FREE0 + sb), sfree[sb] & 1);
+          if (k_ok && s_ok) {
+            if (!(has_draft && i == 0)) ++kf;
+            if (i >= 2) ++sfree[sb];
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kDim / 16; ++kk) {
+              // A = K, K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
+              // B = Q^T, K-major, block-major: 64-dim blocks NQ * 128 B apart, 8-row groups 1 KB apart
+              const uint32_t off = (kk & 3) * 32;
+              umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * 1024 + off, 16, kGroupB),
+                   sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024),
+                   kIdescQK, kk > 0 ? 1u : 0u);
+              if (KV8 && kk == kDim / 32 - 1) umma_commit(bar(K_EMPTY));   // dims 0-127 read
+            }
+            umma_commit(bar(S_FULL0 + sb));
+            umma_commit(bar(KV8 ? K_EMPTY1 : K_EMPTY));
+            ++qk_next;
+            progressed = true;
+          }
+        }
+        // PV of the oldest tile whose P^T is written, one V half at a time
+        if (pv_next < qk_next) {
+          const int t = pv_next;
+          const bool draft = has_draft && t == 0;
+          const bool ready = pv_half == 0 ? mbar_test(bar(P_FULL), pf & 1) && (draft || mbar_test(bar(V_FULL0), vf0 & 1))
+                                          : mbar_test(bar(V_FULL1), vf1 & 1);
+          if (ready) {
+            if (pv_half == 0) {
+              ++pf;
+              if (!draft) ++vf0;
+            } else {
+              ++vf1;
+            }
+            tc_fence_after();
+            // O^T += V^T . P^T over 16-token steps j0 .. j0 + steps - 1
+            auto issue_pv = [&](const int j0, const int steps) {
+#pragma unroll
+              for (int jj = 0; jj < steps; ++jj) {
+                const int j = j0 + jj;
+                const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
+                // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
+                const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
+                  umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
+                       pb, kIdescPV, acc);
+                }
+              }
+            };
+            if (draft) {
+              // the draft tile holds n_nodes <= 64 token rows: all in the first half
+              issue_pv(0, (n_nodes + 15) >> 4);
+              umma_commit(bar(O_DONE));
+              ++pv_next;
+            } else if (pv_half == 0) {
+              issue_pv(0, kT / 32);
+              umma_commit(bar(V_EMPTY0));
+              pv_half = 1;
+            } else {
+              issue_pv(kT / 32, kT / 32);
+              umma_commit(bar(V_EMPTY1));
+              umma_commit(bar(O_DONE));
+              pv_half = 0;
+              ++pv_next;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = clock64();
+        } else {
+          if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
+            sm->abort = 1;
+            report(p.dev_status, SD_DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    // Columns are processed in groups of 32 in loops that are not unrolled;
+    // S^T is re-read from tensor memory by each pass.
+    const int sw = warp - 2;                 // 0..3
+    // scores to base-2 softmax units; a quantised context tile carries the K scale
+    const float qk_mul = (KV8 && !has_draft) ? kScaleLog2 * p.k_scale : kScaleLog2;
+    const int quarter = warp & 3;            // tensor-memory lane quarter of this warp
+    const int row = quarter * 32 + lane;     // token row of S^T / dim row of O^T
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    // Barrier of the four softmax warps on an mbarrier, so that it is bounded too.
+    int gphase = 0;
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(GROUP));
+      return mbar_spin(bar(GROUP), (uint32_t)(gphase++ & 1), sm, p.dev_status);
+    };
+    auto load_cols = [&](const float* arr, int col, float (&w)[32]) {
+      const float4* src = reinterpret_cast<const float4*>(arr + col);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 t = src[k];
+        w[4 * k] = t.x; w[4 * k + 1] = t.y; w[4 * k + 2] = t.z; w[4 * k + 3] = t.w;
+      }
+    };
+    // Column sums of P, from the bf16 P^T tile this warp wrote (the same
+    // rounded weights the PV product multiplies V with): lane L sums columns
+    // 64a + 8(L%8) .. +7 of atom a over token rows 32 * quarter + L/8 + 4k,
+    // k < 8; the warp's lanes and the four warps are added in the epilogue.
+    float csum[NATOM][8];
+#pragma unroll
+    for (int a = 0; a < NATOM; ++a)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) csum[a][j] = 0.f;
+    const int cs_chunk = lane & 7;
+    // Draft CTA: the tree masks, built while the QK product runs.  Node
+    // `row` walks its root path (its ancestor set), then, after the group
+    // barrier, gathers its descendant set: bit n set when node n has `row` on
+    // its root path (itself included).
+    unsigned long long my_desc = 0ull;
+    bool masks_ok = true;
+    if (has_draft) {
+      if (row < n_nodes) {
+        unsigned long long a = 1ull << row;
+        int d = 0;
+        bool ok = row == 0 ? sm->par[0] == -1 : true;
+        for (int u = row; ok && u > 0; ++d) {
+          const int pu = sm->par[u];
+          ok = pu >= 0 && pu < u;
+          if (ok) a |= 1ull << pu;
+          u = pu;
+        }
+        if (!ok) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << row; d = 0; }
+        sm->anc[row] = a;
+        sm->depth[row] = d;
+      }
+      masks_ok = group_sync();
+      if (row < n_nodes) {
+        // with a window, a descendant n more than W - 1 levels below does not see `row`
+        const int dr = sm->depth[row];
+        for (int n = row; n < n_nodes; ++n)
+          if (W <= 0 || sm->depth[n] - dr < W) my_desc |= ((sm->anc[n] >> row) & 1ull) << n;
+      }
+    }
+    for (int i = 0; i < n_tiles && masks_ok; ++i) {
+      const int sb = i & 1;
+      if (!mbar_spin(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_addr + kColS0 + sb * NQ;
+      const bool draft_tile = has_draft;
+      const int t0 = ctx_begin + i * kT;
+      const int valid = draft_tile ? n_nodes : min(kT, ctx_end - t0);
+      // Visibility of this thread's token row, one bit per column of each
+      // 32-column group: context rows before `valid` see every query column;
+      // in the draft tile, node `row` is seen by the columns of its
+      // descendants (itself included; padding columns see the root only).
+      uint32_t vis[NG];
+#pragma unroll
+      for (int gq = 0; gq < NG; ++gq) {
+        const int ncol = min(32, NQ - gq * 32);
+        vis[gq] = (!draft_tile && row < valid) ? (ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u)) : 0u;
+      }
+      if (!draft_tile && W > 0 && t0 < L - W + 1 + kMaxNodes) {
+        // tiles inside the window's band: column q sees token t0 + row from lo_col[q] on
+        const int tpos = t0 + row;
+#pragma unroll
+        for (int gq = 0; gq < NG; ++gq) {
+          uint32_t bits = 0u;
+#pragma unroll 1
+          for (int e = 0; e < 32; ++e) bits |= (tpos >= sm->lo_col[gq * 32 + e] ? 1u : 0u) << e;
+          vis[gq] &= bits;
+        }
+      }
+      if (draft_tile) {
+        unsigned long long d = my_desc;
+        while (d != 0ull) {
+          const int n = __ffsll((long long)d) - 1;
+          d &= d - 1ull;
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(n * hpc - gq * 32, hpc);
+        }
+        if (row == 0) {
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(rows - gq * 32, NQ - rows);
+        }
+      }
+      // Scores of 32 columns of this thread's token row, base 2, masked to -inf.
+      auto load_scores = [&](int g32, float (&v)[32]) {
+        const uint32_t vm = vis_of(vis, g32);
+        float a[16], cc[16];
+        tmem_ld16(s_addr + g32 * 32, a);
+        const bool second = g32 * 32 + 16 < NQ;
+        if (second) tmem_ld16(s_addr + g32 * 32 + 16, cc);
+        tmem_wait_ld();
+        if (!second) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) cc[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float raw = e < 16 ? a[e] : cc[e - 16];
+          v[e] = ((vm >> e) & 1u) ? raw * qk_mul : -INFINITY;
+        }
+      };
+
+      // Pass 1: does any score exceed its column's running maximum by more
+      // than 2^8?  (The first tile always sets the maxima.)
+      bool slow = true;
+      if (i > 0) {
+        float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32], mm[32];
+          load_scores(g32, v);
+          load_cols(sm->m, g32 * 32, mm);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v[e] - mm[e]);
+        }
+        const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
+        if (lane == 0) sm->flag[i & 1][sw] = 0;
+        __syncwarp();
+        if (__any_sync(0xffffffffu, dmax > kThresh) && lane == 0) sm->flag[i & 1][sw] = 1;
+        if (!group_sync()) break;
+        slow = (sm->flag[i & 1][0] | sm->flag[i & 1][1] | sm->flag[i & 1][2] | sm->flag[i & 1][3]) != 0;
+      }
+      bool pv_waited = false;
+      if (slow) {
+        // exact column maxima of this tile, new running maxima and rescale factors
+#pragma unroll 1
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32];
+          load_scores(g32, v);
+          const float mx = transpose_max32(v, lane);
+          sm->red[sw][g32 * 32 + lane] = mx;
+        }
+        if (!group_sync()) break;
+        for (int q = sw * 32 + lane; q < NQ; q += 128) {
+          const float mt = fmaxf(fmaxf(sm->red[0][q], sm->red[1][q]), fmaxf(sm->red[2][q], sm->red[3][q]));
+          const float mo = sm->m[q];
+          const float mn = fmaxf(mo, mt);
+          sm->alpha[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+          sm->m[q] = mn;
+        }
+        if (!group_sync()) break;
+#pragma unroll
+        for (int a = 0; a < NATOM; ++a) {
+          const float4 f0 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[0];
+          const float4 f1 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[1];
+          csum[a][0] *= f0.x; csum[a][1] *= f0.y; csum[a][2] *= f0.z; csum[a][3] *= f0.w;
+          csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
+        }
+        if (i > 0) {
+          // O^T holds earlier tiles: wait for the last PV, then rescale its columns
+          if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+          pv_waited = true;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 2 * NQ / 16; ++c16) {   // O^T low, O^T high
+            float v[16];
+            const int col = c16 % (NQ / 16) * 16;
+            const uint32_t a = tmem + lane_addr + kColO + c16 * 16;
+            tmem_ld16(a, v);
+            const float4* al = reinterpret_cast<const float4*>(sm->alpha + col);
+            float f[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float4 t = al[k];
+              f[4 * k] = t.x; f[4 * k + 1] = t.y; f[4 * k + 2] = t.z; f[4 * k + 3] = t.w;
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= f[e];
+            tmem_st16(a, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      // Pass 2: P = exp2(s - m) as the bf16 P^T row of this token.
+      if (i > 0 && !pv_waited) {
+        if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+      }
+#pragma unroll 1
+      for (int g32 = 0; g32 < NG; ++g32) {
+        float v[32], mm[32];
+        load_scores(g32, v);
+        load_cols(sm->m, g32 * 32, mm);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ch = g32 * 4 + k;      // 16-byte chunk (8 columns) of the P^T row
+          if (ch * 8 < NQ) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = fast_exp2(v[k * 8 + 2 * e] - mm[k * 8 + 2 * e]);
+              const float p1 = fast_exp2(v[k * 8 + 2 * e + 1] - mm[k * 8 + 2 * e + 1]);
+              if constexpr (KV8) {
+                const __half2 h = __floats2half2_rn(p0, p1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              } else {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+            }
+            // MN-major P^T: atom ch/8 (64 columns), token row `row`, 16-byte chunk ch%8
+            *reinterpret_cast<uint4*>(sP + (ch >> 3) * kAtomB + p_off(row, ch & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+      // Column sums of this tile's P from the rows this warp just wrote, while
+      // the PV product runs (the next tile overwrites P^T only after it ends).
+#pragma unroll
+      for (int a = 0; a < NATOM; ++a) {
+        if (a * 64 + cs_chunk * 8 < NQ) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = quarter * 32 + (lane >> 3) + 4 * k;
+            const uint4 pv = *reinterpret_cast<const uint4*>(sP + a * kAtomB + p_off(r, cs_chunk));
+            const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = KV8 ? __half22float2(*reinterpret_cast<const __half2*>(&pw[e]))
+                                   : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
+              csum[a][2 * e] += f.x;
+              csum[a][2 * e + 1] += f.y;
+            }
+          }
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // Each thread owns dims `row` and 128 + `row` of every query column; the
+    // column sums l are the four warps' partial sums, added from shared
+    // memory.  The normalised bf16 rows (the output, or this split's partial
+    // for the merge) are staged in the idle K/V tiles, 256 values per query
+    // column, and leave as 16-byte vector stores.
+    if (!*(volatile int*)&sm->abort) {
+      // add the warp's four row groups (lanes with the same lane % 8), then
+      // publish this warp's column sums
+#pragma unroll
+      for (int a = 0; a < NATOM; ++a)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 8);
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 16);
+        }
+      if (lane < 8) {
+#pragma unroll
+        for (int a = 0; a < NATOM; ++a) {
+          float4* dst = reinterpret_cast<float4*>(sm->lsum[sw] + a * 64 + lane * 8);
+          dst[0] = make_float4(csum[a][0], csum[a][1], csum[a][2], csum[a][3]);
+          dst[1] = make_float4(csum[a][4], csum[a][5], csum[a][6], csum[a][7]);
+        }
+      }
+    }
+    if (!*(volatile int*)&sm->abort && group_sync() &&
+        mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
+      tc_fence_after();
+      const bool direct = nsplit == 1;
+      const float o_mul = (KV8 && !has_draft) ? p.v_scale : 1.0f;   // a quantised context tile: the V scale
+      const size_t part0 = (size_t)s * bd.total_nodes * kHq;
+      const uint32_t t_row = tmem + lane_addr;
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sK);
+#pragma unroll 1
+      for (int col = 0; col < NQ; col += 16) {
+        float lo[16], hi[16], l[16];
+        tmem_ld16(t_row + kColO + col, lo);
+        tmem_ld16(t_row + kColO + NQ + col, hi);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float4 a = reinterpret_cast<const float4*>(sm->lsum[0] + col)[k];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            const float4 b = reinterpret_cast<const float4*>(sm->lsum[w] + col)[k];
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          }
+          l[4 * k] = a.x; l[4 * k + 1] = a.y; l[4 * k + 2] = a.z; l[4 * k + 3] = a.w;
+        }
+        tmem_wait_ld();
+        // every column is written (padding columns too: the staging area holds
+        // NQ rows), so the 16 columns stay independent of each other
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = col + e;
+          const float inv = l[e] > 0.f ? __fdividef(o_mul, l[e]) : 0.f;   // no visible key in this split: 0
+          stage[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
+          stage[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
+        }
+      }
+      // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
+      for (int q = sw * 32 + lane; q < rows; q += 128) {
+        const float lq = sm->lsum[0][q] + sm->lsum[1][q] + sm->lsum[2][q] + sm->lsum[3][q];
+        const float lse2 = sm->m[q] + fast_log2(lq);
+        if (direct) {
+          if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
+        } else {
+          p.lse_part[part0 + sm->outrow[q]] = lse2;
+        }
+      }
+      if (group_sync()) {
+        // 16-byte chunks of the staged 512-byte rows to their output rows, 4 in
+        // flight per thread (the last round repeats the final chunk instead of branching)
+        const int total = rows << 5;
+        uint8_t* gbase = reinterpret_cast<uint8_t*>(direct ? p.out : p.o_part + part0 * kDim);
+        const int t128 = sw * 32 + lane;
+        for (int c0 = t128; c0 - t128 < total; c0 += 4 * 128) {
+          uint4 v[4];
+          int cc[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            cc[u] = min(c0 + u * 128, total - 1);
+            v[u] = *reinterpret_cast<const uint4*>(sK + cc[u] * 16);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const size_t off = ((size_t)sm->outrow[cc[u] >> 5] << 9) + ((cc[u] & 31) << 4);
+            *reinterpret_cast<uint4*>(gbase + off) = v[u];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  }  // compute warps
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm->tmem));
+  }
+}
+
+
+template <int NQ, bool WIN, bool KV8>
+cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, const BatchDesc& bd,
+                      int hpc, int hparts, cudaStream_t st) {
+  const size_t smem = tc_smem_bytes(NQ);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NQ, WIN, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits * kHkv * hparts, bd.batch);
+  cfg.blockDim = dim3(KV8 ? kThreads8 : kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ, WIN, KV8>, mk, mv, p, bd, hpc, hparts);
+}
+
+// Dispatch over the compiled query-column widths (attn_tc.cu: bf16 caches, attn_tc8.cu: e4m3).
+template <bool KV8>
+cudaError_t launch_tc_kind(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, const BatchDesc& bd,
+                           cudaStream_t st) {
+  const TcPlan pl = tc_plan(bd.max_nodes);
+  const bool win = p.window > 0;
+  switch (pl.nq) {
+    case 32: return win ? launch_nq<32, true, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                        : launch_nq<32, false, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st);
+    case 48: return win ? launch_nq<48, true, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                        : launch_nq<48, false, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st);
+    case 64: return win ? launch_nq<64, true, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                        : launch_nq<64, false, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st);
+    case 80: return win ? launch_nq<80, true, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                        : launch_nq<80, false, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st);
+    case 96: return win ? launch_nq<96, true, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st)
+                        : launch_nq<96, false, KV8>(mk, mv, p, bd, pl.hpc, pl.hparts, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+}  // namespace sdv

@@ -13,12 +13,37 @@
 // reported and skipped as a whole.  The copy moves 16-byte vectors: each
 // 512-byte (node, KV head) row of K or V is one warp-wide coalesced read and
 // write.
+//
+// e4m3 caches: the rows are quantised on the way in (the write-time
+// quantisation of «如何在单张 RTX 3090 上让 Qwen3.5-27B token 生成速度提升 6 倍»,
+// 24 GB 显存上的 128K 上下文, here in e4m3 with one scale per layer and tensor):
+// code = e4m3(x * (1 / scale)), the product rounded to fp32, then to the
+// nearest e4m3 value (ties to even), finite values beyond 448 saturating.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sdv {
 namespace {
 
+// Two fp32 values as two e4m3 codes (lo in the low byte), nearest-even, saturating.
+__device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight bf16 (one 16-byte chunk) times `inv`, as eight e4m3 codes.
+__device__ __forceinline__ uint2 quantise8(const uint4 v, float inv) {
+  auto two = [inv](uint32_t w) -> uint32_t {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+    return to_e4m3x2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv));
+  };
+  return make_uint2(two(v.x) | (two(v.y) << 16), two(v.z) | (two(v.w) << 16));
+}
+
+// FP8: e4m3 caches (quantise on the way in); otherwise bf16 rows are copied unchanged.
+template <bool FP8>
 __global__ void __launch_bounds__(256) commit_kernel(const CommitParams p, const BatchDesc bd) {
   const int layer = blockIdx.x;
   const int b = blockIdx.y;
@@ -52,9 +77,28 @@ __global__ void __launch_bounds__(256) commit_kernel(const CommitParams p, const
 
   const uint4* k_src = static_cast<const uint4*>(p.k_new[layer]);
   const uint4* v_src = static_cast<const uint4*>(p.v_new[layer]);
+  constexpr int kVecPerRow = kDim * 2 / 16;  // 32 x 16 B per (node, head) row
+  if constexpr (FP8) {
+    // a 256-code row per (node, head): 32 x 8 B
+    uint2* k_dst = static_cast<uint2*>(p.k_cache[layer]);
+    uint2* v_dst = static_cast<uint2*>(p.v_cache[layer]);
+    const float ki = p.k_inv[layer], vi = p.v_inv[layer];
+    const int tasks = a * kHkv * kVecPerRow;
+    for (int t = threadIdx.x; t < tasks; t += blockDim.x) {
+      const int v = t % kVecPerRow;
+      const int g = (t / kVecPerRow) % kHkv;
+      const int i = t / (kVecPerRow * kHkv);
+      const int pos = L + i;
+      const size_t src = ((size_t)s_src[i] * kHkv + g) * kVecPerRow + v;
+      const size_t dst = (((size_t)s_page[i] * kHkv + g) * kPage + (pos & 15)) * kVecPerRow + v;
+      k_dst[dst] = quantise8(k_src[src], ki);
+      v_dst[dst] = quantise8(v_src[src], vi);
+    }
+    if (layer == 0 && threadIdx.x == 0 && p.new_ctx_lens != nullptr) p.new_ctx_lens[b] = L + a;
+    return;
+  }
   uint4* k_dst = static_cast<uint4*>(p.k_cache[layer]);
   uint4* v_dst = static_cast<uint4*>(p.v_cache[layer]);
-  constexpr int kVecPerRow = kDim * 2 / 16;  // 32 x 16 B per (node, head) row
   const int tasks = a * kHkv * kVecPerRow;
   for (int t = threadIdx.x; t < tasks; t += blockDim.x) {
     const int v = t % kVecPerRow;
@@ -73,7 +117,10 @@ __global__ void __launch_bounds__(256) commit_kernel(const CommitParams p, const
 
 cudaError_t launch_commit(const CommitParams& p, const BatchDesc& bd, cudaStream_t st) {
   dim3 grid(p.num_layers, bd.batch);
-  commit_kernel<<<grid, 256, 0, st>>>(p, bd);
+  if (p.fp8)
+    commit_kernel<true><<<grid, 256, 0, st>>>(p, bd);
+  else
+    commit_kernel<false><<<grid, 256, 0, st>>>(p, bd);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,8 @@ TcPlan tc_plan(int max_nodes);
 size_t tc_smem_bytes(int nq);
 int attn_tc_tile();
 cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+// The same on e4m3 caches (p.k_cache8 / p.v_cache8 with p.k_scale / p.v_scale).
+cudaError_t launch_attn_tc8(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 
 // Log-sum-exp merge of the split partials into the bf16 output.
 cudaError_t launch_attn_merge(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
@@ -54,6 +56,9 @@ struct CommitParams {
   int max_pages;
   int num_pool_pages;
   int num_layers;
+  int fp8;                       // caches hold e4m3 codes: rows are quantised on the way in
+  float k_inv[kMaxLayers];       // fp32 reciprocals of the per-layer K / V scales (fp8 only)
+  float v_inv[kMaxLayers];
 };
 cudaError_t launch_commit(const CommitParams& p, const BatchDesc& bd, cudaStream_t st);
 

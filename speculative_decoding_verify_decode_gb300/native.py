@@ -65,6 +65,9 @@ def load() -> ctypes.CDLL:
     lib.sd_verify_attn_workspace_size.argtypes = [shp]
     lib.sd_verify_attn.restype = ctypes.c_int
     lib.sd_verify_attn.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, fp, vp, sz, vp, vp]
+    lib.sd_verify_attn_fp8.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.sd_verify_attn_fp8.argtypes = [shp, vp, vp, vp, f32, f32, vp, vp, vp, vp, vp, vp, fp, vp, sz, vp, vp]
     lib.sd_verify_attn_noalloc.restype = ctypes.c_int
     lib.sd_verify_attn_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, fp, vp, vp]
     lib.sd_accept_workspace_size.restype = sz
@@ -75,6 +78,10 @@ def load() -> ctypes.CDLL:
     lib.sd_kv_commit.restype = ctypes.c_int
     pp = ctypes.POINTER(ctypes.c_void_p)
     lib.sd_kv_commit.argtypes = [shp, ctypes.c_int, pp, pp, pp, pp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.sd_kv_commit_fp8.restype = ctypes.c_int
+    fpp = ctypes.POINTER(ctypes.c_float)
+    lib.sd_kv_commit_fp8.argtypes = [shp, ctypes.c_int, pp, pp, fpp, fpp, pp, pp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                     vp, vp]
     lib.sd_ddtree_workspace_size.restype = sz
     lib.sd_ddtree_workspace_size.argtypes = [ctypes.c_int] * 4
     lib.sd_ddtree_build.restype = ctypes.c_int
@@ -143,6 +150,18 @@ def sd_verify_attn(shape: Shape, q, k_cache, v_cache, k_new, v_new, page_table, 
            "sd_verify_attn")
 
 
+def sd_verify_attn_fp8(shape: Shape, q, k_cache, v_cache, k_scale: float, v_scale: float, k_new, v_new,
+                       page_table, ctx_lens, parents, out, lse=None, workspace=None, dev_status=None,
+                       stream=None) -> None:
+    """sd_verify_attn over e4m3 caches (uint8 [pool, 4, 16, 256]) with per-tensor scales."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().sd_verify_attn_fp8(shape.ref, _ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                     float(v_scale), _ptr(k_new), _ptr(v_new), _ptr(page_table), _ptr(ctx_lens),
+                                     _ptr(parents), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                     _ptr(dev_status), _stream(stream)),
+           "sd_verify_attn_fp8")
+
+
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -190,6 +209,24 @@ def sd_kv_commit(shape: Shape, k_cache_layers, v_cache_layers, k_new_layers, v_n
                                _ptr(ctx_lens), _ptr(new_ctx_lens), _ptr(accept_len), _ptr(path),
                                int(max_path), _ptr(dev_status), _stream(stream)),
            "sd_kv_commit")
+
+
+def sd_kv_commit_fp8(shape: Shape, k_cache_layers, v_cache_layers, k_scales, v_scales, k_new_layers,
+                     v_new_layers, page_table, ctx_lens, new_ctx_lens, accept_len, path,
+                     max_path: int | None = None, dev_status=None, stream=None) -> None:
+    """sd_kv_commit into e4m3 caches: the accepted rows are quantised with the per-layer scales."""
+    n = len(k_cache_layers)
+    if not (len(v_cache_layers) == len(k_new_layers) == len(v_new_layers) == len(k_scales) == len(v_scales) == n):
+        raise ValueError("per-layer lists differ in length")
+    if max_path is None:
+        max_path = path.shape[-1]
+    ks = (ctypes.c_float * n)(*[float(x) for x in k_scales])
+    vs = (ctypes.c_float * n)(*[float(x) for x in v_scales])
+    _check(load().sd_kv_commit_fp8(shape.ref, n, _ptr_array(k_cache_layers), _ptr_array(v_cache_layers), ks, vs,
+                                   _ptr_array(k_new_layers), _ptr_array(v_new_layers), _ptr(page_table),
+                                   _ptr(ctx_lens), _ptr(new_ctx_lens), _ptr(accept_len), _ptr(path),
+                                   int(max_path), _ptr(dev_status), _stream(stream)),
+           "sd_kv_commit_fp8")
 
 
 def sd_ddtree_workspace_size(batch: int, positions: int, vocab: int, topk: int) -> int:

@@ -19,7 +19,9 @@ class VerifyStep:
 
     def __init__(self, q_indptr, max_pages_per_seq: int, num_pool_pages: int, num_layers: int, vocab: int,
                  device="cuda", num_splits: int = 0, max_path: int | None = None, want_lse: bool = False,
-                 window: int = 0):
+                 window: int = 0, k_scales=None, v_scales=None):
+        """``k_scales`` / ``v_scales`` (per-layer floats) select e4m3 caches: attention reads the codes with
+        these scales and the commit quantises the accepted rows with them."""
         self.q_indptr = np.asarray(q_indptr, dtype=np.int32)
         self.batch = len(self.q_indptr) - 1
         self.total = int(self.q_indptr[-1])
@@ -27,6 +29,11 @@ class VerifyStep:
         self.vocab = int(vocab)
         self.device = torch.device(device)
         self.shape = native.Shape(self.q_indptr, max_pages_per_seq, num_pool_pages, num_splits, window)
+        self.fp8 = k_scales is not None
+        if self.fp8 and (v_scales is None or len(k_scales) != self.num_layers or len(v_scales) != self.num_layers):
+            raise ValueError("e4m3 caches need one K and one V scale per layer")
+        self.k_scales = None if k_scales is None else [float(x) for x in k_scales]
+        self.v_scales = None if v_scales is None else [float(x) for x in v_scales]
         self.max_path = int(max_path or int(np.diff(self.q_indptr).max()))
         dev = self.device
         ws = native.sd_verify_attn_workspace_size(self.shape)
@@ -45,9 +52,14 @@ class VerifyStep:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def attention(self, layer, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, stream=None):
-        native.sd_verify_attn(self.shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents,
-                              self.out[layer], None if self.lse is None else self.lse[layer], self.attn_ws,
-                              self.dev_status, stream)
+        lse = None if self.lse is None else self.lse[layer]
+        if self.fp8:
+            native.sd_verify_attn_fp8(self.shape, q, k_cache, v_cache, self.k_scales[layer], self.v_scales[layer],
+                                      k_new, v_new, page_table, ctx_lens, parents, self.out[layer], lse,
+                                      self.attn_ws, self.dev_status, stream)
+        else:
+            native.sd_verify_attn(self.shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents,
+                                  self.out[layer], lse, self.attn_ws, self.dev_status, stream)
 
     def accept(self, logits, parents, draft_tokens, stream=None):
         native.sd_accept(self.q_indptr, self.vocab, logits, parents, draft_tokens, self.accept_len, self.path,
@@ -55,6 +67,11 @@ class VerifyStep:
                          stream)
 
     def commit(self, k_caches, v_caches, k_news, v_news, page_table, ctx_lens, stream=None):
+        if self.fp8:
+            native.sd_kv_commit_fp8(self.shape, k_caches, v_caches, self.k_scales, self.v_scales, k_news, v_news,
+                                    page_table, ctx_lens, self.new_ctx_lens, self.accept_len, self.path,
+                                    self.max_path, self.dev_status, stream)
+            return
         native.sd_kv_commit(self.shape, k_caches, v_caches, k_news, v_news, page_table, ctx_lens,
                             self.new_ctx_lens, self.accept_len, self.path, self.max_path, self.dev_status,
                             stream)

@@ -38,6 +38,11 @@ Recipe (stated once, used by tests and bench):
 * DDTree: spine depth D ~ U[8, 16] under the root, the remaining nodes hang off
   random nodes with < 3 children and depth < 16, renumbered breadth-first so
   that ``parent[j] < j``; only spine drafts are planted.
+* e4m3 (FP8) caches: random codes drawn field by field, sign ~ U{0, 1},
+  exponent field round(N(7, 1.2)) clipped to [0, 15], mantissa ~ U{0..7}
+  (the NaN pattern, exponent 15 with mantissa 7, becomes mantissa 6); one scale
+  per layer and tensor, 2^-5.5 * U(0.75, 1.25), which puts the typical cache
+  value near the bf16 recipe's 1/16.  Q and the draft block's K/V stay bf16.
 """
 from __future__ import annotations
 
@@ -76,6 +81,9 @@ class Workload:
     v_cache: list = field(default_factory=list)
     logits: torch.Tensor | None = None           # fp32 [sum N, V]
     window: int = 0                              # sliding window (0: the whole context)
+    kv: str = "bf16"                             # cache format: "bf16", or "fp8" (e4m3 codes, uint8)
+    k_scales: list = field(default_factory=list)  # fp8: per layer K / V scale (python floats)
+    v_scales: list = field(default_factory=list)
 
     @property
     def total_nodes(self) -> int:
@@ -105,6 +113,13 @@ CONFIGS = {
     # sliding-window verify: attention over the most recent 2,048 positions of a long context
     "chain8_ctx32k_win2048": dict(batch=1, layers=16, ctx=32768, tree="chain", K=8, vocab=151936,
                                   p=0.8, seed=12, table="permuted", window=2048),
+    # quantised (e4m3) KV caches: the long-context trees and the 4K chain
+    "ddtree22_ctx32k_fp8": dict(batch=1, layers=16, ctx=32768, tree="ddtree", budget=22,
+                                vocab=151936, p=0.85, seed=3, table="permuted", kv="fp8"),
+    "ddtree22_ctx128k_fp8": dict(batch=1, layers=16, ctx=131072, tree="ddtree", budget=22,
+                                 vocab=151936, p=0.85, seed=5, table="permuted", kv="fp8"),
+    "chain8_ctx4k_fp8": dict(batch=1, layers=16, ctx=4096, tree="chain", K=8, vocab=151936,
+                             p=0.8, seed=12, table="permuted", kv="fp8"),
 }
 
 
@@ -238,6 +253,17 @@ def _randn_bf16(gen: torch.Generator, shape, scale: float, device) -> torch.Tens
     return (x * scale).to(torch.bfloat16)
 
 
+def random_e4m3_codes(gen: torch.Generator, shape, device) -> torch.Tensor:
+    """uint8 e4m3 codes drawn field by field (sign, exponent ~ round(N(7, 1.2)) in [0, 15],
+    mantissa uniform); the NaN pattern (exponent 15, mantissa 7) is replaced by mantissa 6."""
+    sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32)
+    e = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).mul_(1.2).add_(7.0)
+    e = e.round_().clamp_(0, 15).to(torch.int32)
+    m = torch.randint(0, 8, shape, generator=gen, device=device, dtype=torch.int32)
+    m = torch.where((e == 15) & (m == 7), torch.full_like(m, 6), m)
+    return (sign * 128 + e * 8 + m).to(torch.uint8)
+
+
 def fill_tensors(w: Workload, layers: int, seed: int, device="cpu", qkv_scale: float = 1.0 / 16,
                  logits: bool = True) -> Workload:
     """Draw Q, draft K/V, paged K/V caches and logits for ``layers`` layers."""
@@ -246,12 +272,21 @@ def fill_tensors(w: Workload, layers: int, seed: int, device="cpu", qkv_scale: f
     n = w.total_nodes
     w.layers = layers
     w.q, w.k_new, w.v_new, w.k_cache, w.v_cache = [], [], [], [], []
+    w.k_scales, w.v_scales = [], []
+    srng = np.random.default_rng(int(seed) * 7919 + 3)
+    cache_shape = (w.num_pool_pages, H_KV, PAGE, HEAD_DIM)
     for _ in range(layers):
         w.q.append(_randn_bf16(gen, (n, H_Q, HEAD_DIM), qkv_scale, device))
         w.k_new.append(_randn_bf16(gen, (n, H_KV, HEAD_DIM), qkv_scale, device))
         w.v_new.append(_randn_bf16(gen, (n, H_KV, HEAD_DIM), qkv_scale, device))
-        w.k_cache.append(_randn_bf16(gen, (w.num_pool_pages, H_KV, PAGE, HEAD_DIM), qkv_scale, device))
-        w.v_cache.append(_randn_bf16(gen, (w.num_pool_pages, H_KV, PAGE, HEAD_DIM), qkv_scale, device))
+        if w.kv == "fp8":
+            w.k_cache.append(random_e4m3_codes(gen, cache_shape, device))
+            w.v_cache.append(random_e4m3_codes(gen, cache_shape, device))
+            w.k_scales.append(float(2.0 ** -5.5 * srng.uniform(0.75, 1.25)))
+            w.v_scales.append(float(2.0 ** -5.5 * srng.uniform(0.75, 1.25)))
+        else:
+            w.k_cache.append(_randn_bf16(gen, cache_shape, qkv_scale, device))
+            w.v_cache.append(_randn_bf16(gen, cache_shape, qkv_scale, device))
     if logits:
         lg = torch.randn((n, w.vocab), generator=gen, device=device, dtype=torch.float32)
         lg.clamp_(-5.5, 5.5)
@@ -263,11 +298,11 @@ def fill_tensors(w: Workload, layers: int, seed: int, device="cpu", qkv_scale: f
 
 
 def make_workload(name: str, device="cpu", layers: int | None = None, qkv_scale: float = 1.0 / 16,
-                  ctx_override=None, logits: bool = True, rescue: bool = False) -> Workload:
+                  ctx_override=None, logits: bool = True, rescue: bool = False, kv: str | None = None) -> Workload:
     """Build one of the named workloads in ``CONFIGS``.
 
     ``layers`` and ``ctx_override`` shrink a workload for quick checks while
-    keeping its tree, table mode and seed.
+    keeping its tree, table mode and seed; ``kv`` overrides the cache format.
     """
     cfg = CONFIGS[name]
     rng = np.random.default_rng(cfg["seed"])
@@ -296,6 +331,7 @@ def make_workload(name: str, device="cpu", layers: int | None = None, qkv_scale:
                        planted_list, table=cfg["table"], rescue=rescue, rng=rng)
     w.name = name
     w.window = int(cfg.get("window", 0))
+    w.kv = kv if kv is not None else cfg.get("kv", "bf16")
     nl = cfg["layers"] if layers is None else layers
     return fill_tensors(w, nl, cfg["seed"], device=device, qkv_scale=qkv_scale, logits=logits)
 

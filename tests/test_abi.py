@@ -133,3 +133,22 @@ def test_negative_window_is_rejected(lib):
     s.c.window = -1
     assert _attn(lib, s) == native.SD_ERR_INVALID_ARG
     assert lib.sd_verify_attn_workspace_size(s.ref) == 0
+
+
+def test_fp8_scales_checked_before_any_launch(lib):
+    s = _shape()
+    attn = lambda ks, vs, kc=FAKE: lib.sd_verify_attn_fp8(s.ref, FAKE, kc, FAKE, ks, vs, FAKE, FAKE, FAKE, FAKE,
+                                                          FAKE, FAKE, None, None, 0, None, None)
+    for bad in (0.0, -1.0, float("inf"), float("nan"), 1e-45):     # 1e-45: the reciprocal overflows fp32
+        assert attn(bad, 1.0) == native.SD_ERR_INVALID_ARG, bad
+        assert attn(1.0, bad) == native.SD_ERR_INVALID_ARG, bad
+    assert attn(1.0, 1.0, kc=FAKE + 4) == native.SD_ERR_INVALID_ARG   # codes must start on 16 bytes
+    assert attn(1.0, 1.0, kc=None) == native.SD_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    good = (ctypes.c_float * 2)(0.5, 0.25)
+    bad = (ctypes.c_float * 2)(0.5, 0.0)
+    commit = lambda ks, vs: lib.sd_kv_commit_fp8(s.ref, 2, arr, arr, ks, vs, arr, arr, FAKE, FAKE, None, FAKE,
+                                                 FAKE, 8, None, None)
+    assert commit(None, good) == native.SD_ERR_INVALID_ARG
+    assert commit(good, bad) == native.SD_ERR_INVALID_ARG
+    assert commit(bad, good) == native.SD_ERR_INVALID_ARG
