@@ -33,7 +33,8 @@ from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inp
 
 METRIC = "verify steps/s"
 DEFAULT_CONFIG = "chain8_ctx4k"
-ATTN_SRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", "attn_tc.cu")
+ATTN_SRCS = [os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", f)
+             for f in ("attn_tc_kernel.cuh", "attn_tc.cu", "attn_tc8.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
 
 
@@ -49,9 +50,10 @@ def peaks():
 def attn_bytes_per_layer(w) -> int:
     """Algorithmic bytes of one layer's verify attention.
 
-    Context K and V are read once (2 x 4 heads x 256 x 2 B = 4096 B per token),
-    plus Q, the draft K/V, the output and the page-table entries.  With a
-    sliding window W only the W - 1 most recent context tokens are visible.
+    Context K and V are read once (2 x 4 heads x 256 x 2 B = 4096 B per token;
+    2048 B with e4m3 caches), plus Q, the draft K/V, the output and the
+    page-table entries.  With a sliding window W only the W - 1 most recent
+    context tokens are visible.
     """
     lens = [int(L) for L in w.ctx_lens]
     if getattr(w, "window", 0):
@@ -59,12 +61,16 @@ def attn_bytes_per_layer(w) -> int:
     ctx = sum(lens)
     pages = int(sum((L + 15) // 16 for L in lens))
     n = w.total_nodes
-    return ctx * 4096 + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
+    per_token = 2048 if getattr(w, "kv", "bf16") == "fp8" else 4096
+    return ctx * per_token + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
 
 
 def kernel_sha() -> str:
-    with open(ATTN_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+    h = hashlib.sha256()
+    for src in ATTN_SRCS:
+        with open(src, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
 
 
 def traffic_for(config: str):
@@ -195,8 +201,10 @@ def run_ours(args, world, rank, local):
     native.load()
     w = synth.make_workload(args.config, device=dev, layers=args.layers or None)
     d = device_inputs(w, dev)
+    fp8 = w.kv == "fp8"
     step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev,
-                      num_splits=args.splits, window=w.window)
+                      num_splits=args.splits, window=w.window, k_scales=w.k_scales if fp8 else None,
+                      v_scales=w.v_scales if fp8 else None)
     run_args = (w.q, w.k_cache, w.v_cache, w.k_new, w.v_new, d["page_table"], d["ctx_lens"], d["parents"],
                 d["draft_tokens"], w.logits)
     step.run(*run_args)                       # eager once: surfaces launch errors early
@@ -286,9 +294,11 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded; Q/K/V ~ N(0,1)/16 bf16, planted-argmax fp32 logits)",
-        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "window": w.window,
+        "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16",
+        "data": ("synthetic (seeded; Q and draft K/V ~ N(0,1)/16 bf16, random e4m3 cache codes with per-layer "
+                 "scales, planted-argmax fp32 logits)" if fp8 else
+                 "synthetic (seeded; Q/K/V ~ N(0,1)/16 bf16, planted-argmax fp32 logits)"),
+        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "window": w.window, "kv": w.kv,
                    "ctx_lens": [int(x) for x in w.ctx_lens][:8], "draft_nodes": w.total_nodes,
                    "vocab": w.vocab, "heads": "24q/4kv", "head_dim": 256, "page": 16,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -321,23 +331,35 @@ def cpu_baseline(w, config: str, reps: int = 1) -> dict:
     A step is extrapolated as layers x attention + accept + commit.
     """
     import oracle
+    import oracle.fp8_oracle as fp8_oracle
     f32 = lambda t: t.detach().to("cpu", torch.float32).numpy()
     layer = 0
-    host = dict(q=f32(w.q[layer]), kc=f32(w.k_cache[layer]), vc=f32(w.v_cache[layer]),
+    fp8 = w.kv == "fp8"
+    cache = (lambda t: t.detach().cpu().numpy()) if fp8 else f32
+    host = dict(q=f32(w.q[layer]), kc=cache(w.k_cache[layer]), vc=cache(w.v_cache[layer]),
                 kn=f32(w.k_new[layer]), vn=f32(w.v_new[layer]))
     logits = w.logits.detach().cpu().numpy()
     t_attn, t_acc, t_com = [], [], []
     for _ in range(reps):
         t = time.perf_counter()
-        oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
-                                w.ctx_lens, w.q_indptr, w.parents, window=w.window or None)
+        if fp8:
+            fp8_oracle.verify_attention_fp8(host["q"], host["kc"], host["vc"], w.k_scales[layer], w.v_scales[layer],
+                                            host["kn"], host["vn"], w.page_table, w.ctx_lens, w.q_indptr,
+                                            w.parents, window=w.window or None)
+        else:
+            oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
+                                    w.ctx_lens, w.q_indptr, w.parents, window=w.window or None)
         t_attn.append(time.perf_counter() - t)
         t = time.perf_counter()
         _, lens, paths, _ = oracle.accept(w.q_indptr, w.parents, w.draft_tokens, logits)
         t_acc.append(time.perf_counter() - t)
         t = time.perf_counter()
-        oracle.kv_commit([host["kc"]], [host["vc"]], [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens,
-                         w.q_indptr, lens, paths)
+        if fp8:
+            fp8_oracle.kv_commit_fp8([host["kc"]], [host["vc"]], [w.k_scales[layer]], [w.v_scales[layer]],
+                                     [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens, w.q_indptr, lens, paths)
+        else:
+            oracle.kv_commit([host["kc"]], [host["vc"]], [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens,
+                             w.q_indptr, lens, paths)
         t_com.append(time.perf_counter() - t)
     step_s = w.layers * statistics.mean(t_attn) + statistics.mean(t_acc) + w.layers * statistics.mean(t_com)
     return {"value": 1.0 / step_s, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -361,7 +383,7 @@ def run_reference(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "vocab": w.vocab,
-                       "window": w.window},
+                       "window": w.window, "kv": w.kv},
             "impl": "reference", "cpu_baseline": {**base, "wall_s": wall},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

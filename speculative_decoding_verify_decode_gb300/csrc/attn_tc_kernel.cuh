@@ -43,15 +43,18 @@
 // scale per tensor (K, V) of the layer; the key and value a code stands for is
 // decode(code) * scale (the quantised KV cache of «如何在单张 RTX 3090 上让
 // Qwen3.5-27B token 生成速度提升 6 倍», 24 GB 显存上的 128K 上下文, here in e4m3).
-// Four converter warps (0 and 7 for K, 6 and 8 for V) take the producers'
-// place: each loads its pages of the next tile into registers with 16-byte
-// loads as soon as it has stored the current one (the register file is a
-// second tile buffer), waits for the tile buffer to be released, widens the
-// codes to f16 (every e4m3 value is exact in f16) in the same group-major
-// swizzled layout, and signals the MMA.  Q^T, P^T and the draft block are f16
-// too, so the products are kind::f16 with f16 operands.  The K scale joins
-// the softmax multiplier and the V scale the epilogue's normalisation; the
-// draft block (not yet committed, so not quantised) has scale 1.
+// The tensor core takes f16 operands (every e4m3 value is exact in f16), so
+// each tile passes through two stages: a loader warp (9) brings e4m3 half
+// tiles by TMA into two 16 KB staging slots per tensor (K: dims 0-127 or
+// 128-255 of every token, one 2 KB box per page; V: pages 0-3 or 4-7, one
+// 4 KB bulk copy per page), and converter warps (0 and 7 for K, 6 and 8 for
+// V) widen a slot into the tensor's single f16 half-tile buffer, which the
+// MMA consumes half by half (QK in two 128-dim steps, PV in two 64-token
+// steps).  A slot is refilled as soon as it has been widened, so the next
+// tile's codes are in flight while this tile is multiplied.  Q^T, P^T and the
+// draft block are f16 too.  The K scale joins the softmax multiplier and the
+// V scale the epilogue's normalisation; the draft block (not yet committed,
+// so not quantised) has scale 1.
 #pragma once
 
 #include <cstddef>
@@ -71,9 +74,11 @@ constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 25
 constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
 constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
 constexpr int kThreads = 224;
-constexpr int kThreads8 = 288;          // the quantised-cache instances: two more converter warps
+constexpr int kThreads8 = 320;          // the quantised-cache instances: two more converters and a loader
 constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
-constexpr int kWarpK2 = 7, kWarpV2 = 8;  // second K / V converter warp (quantised cache)
+constexpr int kWarpK2 = 7, kWarpV2 = 8, kWarpLoad = 9;   // quantised cache: second K / V converter, TMA loader
+constexpr int kHalfB = kTileB / 2;      // quantised cache: f16 half tile (128 tokens x 128 dims, or 64 x 256)
+constexpr int kSlotB = kTileB / 4;      // quantised cache: e4m3 half tile (staging slot)
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
 constexpr float kNoMax = -1.0e30f;      // the running maximum before any visible score
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
@@ -81,10 +86,10 @@ constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 cloc
 // The V tile moves in two 64-token halves (pages 0-3 and 4-7, each 32 KB
 // contiguous), so that the first half of the next tile loads while the PV
 // product still reads the second half of this one.
-// A quantised K tile is also filled and released in two halves of the head
-// dimension (K_FULL / K_EMPTY: dims 0-127, K_FULL1 / K_EMPTY1: dims 128-255).
+// Quantised cache: K_FULL / K_EMPTY and V_FULL0 / V_EMPTY0 guard the f16
+// half-tile buffers (two phases per tile), K8_* / V8_* the e4m3 staging slots.
 enum Bar { K_FULL, K_EMPTY, V_FULL0, V_FULL1, V_EMPTY0, V_EMPTY1, S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, O_DONE,
-           GROUP, K_FULL1, K_EMPTY1, NUM_BARS };
+           GROUP, K8_FULL0, K8_FULL1, K8_EMPTY0, K8_EMPTY1, V8_FULL0, V8_FULL1, V8_EMPTY0, V8_EMPTY1, NUM_BARS };
 
 constexpr int kCols = 128;   // per-column arrays padded to whole 32-column groups
 constexpr int kMaxStageRows = kTcMaxNQ + 2 * kMaxNodes;   // Q^T rows + the draft block's K and V rows
@@ -293,35 +298,27 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
   };
   return make_uint4(one(v.x), one(v.y), one(v.z), one(v.w));
 }
-// Two e4m3 codes (low byte first) as two f16 (exact: e4m3 is a subset of f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(two & 0xffffu)));
-  return r;
+// Four e4m3 codes (one 32-bit word, low byte first) as four f16 (two words;
+// exact: e4m3 is a subset of f16).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
-// 16 bytes of a streamed cache page; no L1 allocation (each page is read once per CTA).
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// Half a page of e4m3 K codes (16 slots x 128 dims: x = 0 or 128) into shared
+// memory: a 2 KB box of the 3-D code map at (x, 0, page * 4 + head).
+__device__ __forceinline__ void tma_load_k8(uint32_t dst, const CUtensorMap* map, int x, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(0), "r"(z), "r"(bar)
+      : "memory");
 }
-// 16 e4m3 codes (dims 16c .. 16c + 15 of token row r) widened into the two
-// f16 chunks 2c and 2c + 1 of a group-major K/V tile.  Lanes whose chunk has
-// bit 2 set store the odd chunk first, so that each group of 8 lanes (one row,
-// two 64-dim blocks) covers all 32 banks in both stores.
-__device__ __forceinline__ void store_widened(uint8_t* tile, int r, int c, const uint4 v) {
-  const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
-                              e4m3x2_to_f16x2(v.y >> 16));
-  const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
-                              e4m3x2_to_f16x2(v.w >> 16));
-  const bool odd_first = (c & 4) != 0;
-  const uint32_t a_lo = kv_off(r, 2 * c), a_hi = kv_off(r, 2 * c + 1);
-  *reinterpret_cast<uint4*>(tile + (odd_first ? a_hi : a_lo)) = odd_first ? hi : lo;
-  *reinterpret_cast<uint4*>(tile + (odd_first ? a_lo : a_hi)) = odd_first ? lo : hi;
+// `bytes` contiguous bytes (a multiple of 16, both addresses 16-byte aligned) into shared memory.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
-
 // Bits [start, start + len) of a 32-bit word (clipped to the word).
 __device__ __forceinline__ uint32_t bit_range(int start, int len) {
   const int a = max(start, 0), e = min(start + len, 32);
@@ -374,14 +371,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   uint8_t* sQ = dyn_smem;
   uint8_t* sK = sQ + kQB;
-  uint8_t* sV = sK + kTileB;
-  uint8_t* sP = sV + kTileB;
+  uint8_t* sV = sK + (KV8 ? kHalfB : kTileB);
+  uint8_t* sK8 = sV + kHalfB;        // quantised cache: two e4m3 K slots
+  uint8_t* sV8 = sK8 + 2 * kSlotB;   // quantised cache: two e4m3 V slots
+  uint8_t* sP = sK + 2 * kTileB;
   Small* sm = reinterpret_cast<Small*>(sP + NATOM * kAtomB);
 
   constexpr int NT = KV8 ? kThreads8 : kThreads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // warps that fill the K/V tiles: TMA producers, or converters for a quantised cache
-  const bool producer = warp == kWarpK || warp == kWarpV || (KV8 && (warp == kWarpK2 || warp == kWarpV2));
+  const bool producer =
+      warp == kWarpK || warp == kWarpV || (KV8 && (warp == kWarpK2 || warp == kWarpV2 || warp == kWarpLoad));
   const int bid = blockIdx.x;
   const int c = bid % hparts;
   const int g = (bid / hparts) % kHkv;
@@ -395,8 +395,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // stream before touching global memory, then let the merge kernel's blocks
   // be scheduled (they wait for this grid to finish before reading).
   // the producers fetch their TMA descriptor while the rest of the prologue runs
-  if (!KV8 && (warp == kWarpK || warp == kWarpV) && lane == 0)
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpK ? &tm_k : &tm_v))
+  if (((!KV8 && (warp == kWarpK || warp == kWarpV)) || (KV8 && warp == kWarpLoad)) && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpV ? &tm_v : &tm_k))
                  : "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -436,7 +436,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NUM_BARS; ++i) {
       // a quantised tile is complete when both of its converter warps have arrived
-      const bool conv = KV8 && (i == K_FULL || i == K_FULL1 || i == V_FULL0 || i == V_FULL1);
+      const bool conv = KV8 && (i == K_FULL || i == V_FULL0 || i == K8_EMPTY0 || i == K8_EMPTY1 ||
+                                i == V8_EMPTY0 || i == V8_EMPTY1);
       const uint32_t cnt = (i == S_FREE0 || i == S_FREE1 || i == P_FULL || i == GROUP) ? 4u : conv ? 2u : 1u;
       mbar_init(smem_u32(&sm->bar[i]), cnt);
     }
@@ -522,61 +523,175 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
 
   if (KV8 && producer) {
-    // ------------------------------------------------------------ converters (quantised cache)
-    // Each tile is converted in two halves, each held in registers (16 loads
-    // of 16 bytes per lane) while the half's buffer may still be in use:
-    //   K half h: dims 128h .. 128h + 127 of every token row (QK steps 8h ..
-    //     8h + 7); warp wi takes pages wi + 2j (j < 4); lane l: slot l/8 + 4u,
-    //     16-byte chunk l%8 + 8h, so 8 lanes read one 128-byte half row;
-    //   V half h: pages 4h .. 4h + 3 (the 64-token halves the PV product
-    //     consumes); warp wi takes pages 4h + wi + 2j (j < 2); lane l: slot
-    //     l/16 + 2u, chunk l%16, so 16 lanes read one 256-byte row.
-    const bool is_k = warp == kWarpK || warp == kWarpK2;
-    const int wi = (warp == kWarpK || warp == kWarpV) ? 0 : 1;
-    uint8_t* dst = is_k ? sK : sV;
-    const uint8_t* cache = is_k ? p.k_cache8 : p.v_cache8;
     const int n_ctx = has_draft ? 0 : n_tiles;
-    int page_next = page0;
-    auto publish = [&](uint32_t full) {
-      fence_async_smem();   // plain stores, read by the tensor core
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full);
-    };
-    bool ok = true;
-    for (int i = 0; i < n_ctx && ok; ++i) {
+    int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
+    // page ids of tile i (lanes 0-7; -1: not needed, or outside the pool)
+    auto tile_pages = [&](int i, int& valid, bool report_bad) -> int {
       const int t0 = ctx_begin + i * kT;
-      const int valid = min(kT, ctx_end - t0);
+      valid = min(kT, ctx_end - t0);
       int page = (lane < 8 && lane * kPage < valid) ? page_next : -1;
       if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
         page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
       if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
-        report(p.dev_status, SD_DEV_BAD_PAGE);
+        if (report_bad) report(p.dev_status, SD_DEV_BAD_PAGE);
         page = -1;
       }
-      const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
-      for (int h = 0; h < 2 && ok; ++h) {
-        uint4 v[16];
-        int row[16], chunk[16];
+      return page;
+    };
+    if (warp == kWarpLoad) {
+      // ---------------------------------------------------------- loader (quantised cache)
+      // Per tile, four half-tile loads (K dims 0-127, K dims 128-255, V pages
+      // 0-3, V pages 4-7), each issued as soon as its slot has been widened.
+      int last[4] = {-1, -1, -1, -1};
+      bool ok = true;
+      for (int i = 0; i < n_ctx && ok; ++i) {
+        int valid;
+        const int page = tile_pages(i, valid, true);
+        const uint32_t need = __ballot_sync(0xffffffffu, lane < 8 && page >= 0);
+        const uint32_t parity = (uint32_t)(i & 1) ^ 1u;
+        int todo = 0xF;
+        long long idle_since = clock64();
+        while (todo != 0) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int pi = is_k ? wi + 2 * (k >> 2) : 4 * h + wi + 2 * (k >> 3);
-          const int slot = is_k ? (lane >> 3) + 4 * (k & 3) : (lane >> 4) + 2 * (k & 7);
-          chunk[k] = is_k ? (lane & 7) + 8 * h : (lane & 15);
-          row[k] = pi * kPage + slot;
-          const int pg = __shfl_sync(0xffffffffu, page, pi);
-          const bool in = pg >= 0 && row[k] < valid;
-          v[k] = in ? ld_stream16(cache + (((size_t)pg * kHkv + g) * kPage + slot) * kDim + chunk[k] * 16)
-                    : make_uint4(0, 0, 0, 0);
+          for (int part = 0; part < 4; ++part) {
+            const bool is_k = part < 2;
+            const int h = part & 1;
+            if (!(todo & (1 << part))) continue;
+            const uint32_t empty = bar(is_k ? K8_EMPTY0 + h : V8_EMPTY0 + h);
+            const uint32_t full = bar(is_k ? K8_FULL0 + h : V8_FULL0 + h);
+            const bool ready = __shfl_sync(0xffffffffu, lane == 0 ? (mbar_test(empty, parity) ? 1 : 0) : 0, 0) != 0;
+            if (!ready) continue;
+            const uint32_t pm = is_k ? need : (need & (0xFu << (4 * h)));
+            if (lane == 0) mbar_expect_tx(full, (uint32_t)__popc(pm) * (is_k ? kSlotB / 8 : kSlotB / 4));
+            __syncwarp();
+            if ((pm >> lane) & 1u) {
+              if (is_k)
+                tma_load_k8(smem_u32(sK8 + h * kSlotB + lane * (kSlotB / 8)), &tm_k, 128 * h, page * kHkv + g, full);
+              else
+                bulk_load(smem_u32(sV8 + h * kSlotB + (lane - 4 * h) * (kSlotB / 4)),
+                          p.v_cache8 + ((size_t)page * kHkv + g) * (kPage * kDim), kSlotB / 4, full);
+            }
+            todo &= ~(1 << part);
+            last[part] = i;
+            idle_since = clock64();
+          }
+          if (todo != 0) {
+            if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
+              if (lane == 0) { sm->abort = 1; report(p.dev_status, SD_DEV_TIMEOUT); }
+              ok = false;
+              break;
+            }
+            __nanosleep(20);
+          }
         }
-        const uint32_t empty = bar(is_k ? (h == 0 ? K_EMPTY : K_EMPTY1) : (h == 0 ? V_EMPTY0 : V_EMPTY1));
-        if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) store_widened(dst, row[k], chunk[k], v[k]);
-        publish(bar(is_k ? (h == 0 ? K_FULL : K_FULL1) : (h == 0 ? V_FULL0 : V_FULL1)));
       }
-      if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
+      // no copy may still be landing when the CTA ends (after an abort): wait, bounded, for the last of each slot
+      if (lane == 0) {
+        for (int part = 0; part < 4; ++part) {
+          if (last[part] < 0) continue;
+          const uint32_t full = bar(part < 2 ? K8_FULL0 + (part & 1) : V8_FULL0 + (part & 1));
+          const long long t0 = clock64();
+          while (!mbar_test(full, (uint32_t)(last[part] & 1)) && clock64() - t0 < kWaitCycles) {
+          }
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- converters (quantised cache)
+      // Warp wi (0 or 1) of a tensor, thread t = 32 wi + lane, widens 16
+      // chunks of 16 codes of a slot:
+      //   K: token rows t/8 + 8u (u < 16), dims 16 (t%8) .. +15 of the half;
+      //   V: token rows t/16 + 4u of the half (64 rows), dims 16 (t%16) .. +15.
+      // Both slot layouts are linear in the row (K 128 B, V 256 B per row), so
+      // each step moves the source by 1 KB and the destination by a constant
+      // (K: one 8-row group, 2 KB; V: every other step one 8-row group, 4 KB,
+      // the swizzle row alternating between t/16 and t/16 + 4).  Each 8-lane
+      // group reads 128 contiguous bytes and writes one row's 16-byte chunks
+      // (the odd chunk first where bit 2 of the chunk is set: no bank conflicts).
+      const bool is_k = warp == kWarpK || warp == kWarpK2;
+      const int t64 = ((warp == kWarpK || warp == kWarpV) ? 0 : 32) + lane;
+      uint8_t* dst = is_k ? sK : sV;
+      const int c = is_k ? (t64 & 7) : (t64 & 15);           // 16-code chunk of the row
+      const int r0 = is_k ? (t64 >> 3) : (t64 >> 4);          // first row
+      const bool odd_first = (c & 4) != 0;
+      const uint32_t src0 = (uint32_t)(r0 * (is_k ? 128 : kDim) + c * 16);
+      // destination of the first / second stored chunk for rows with r % 8 = rr, group 0
+      auto dst_pair = [&](int rr, uint32_t& d_first, uint32_t& d_second) {
+        const int cc_first = 2 * c + (odd_first ? 1 : 0), cc_second = 2 * c + (odd_first ? 0 : 1);
+        auto off = [&](int cc) { return (uint32_t)((cc >> 3) * 1024 + rr * 128 + (((cc & 7) ^ rr) << 4)); };
+        d_first = off(cc_first);
+        d_second = off(cc_second);
+      };
+      uint32_t d1e, d2e, d1o, d2o;   // even / odd steps (V: the swizzle row alternates)
+      dst_pair(r0 & 7, d1e, d2e);
+      dst_pair(is_k ? (r0 & 7) : ((r0 + 4) & 7), d1o, d2o);
+      const uint32_t dst_base = smem_u32(dst);
+      bool ok = true;
+      int uses = 0;   // phases of the f16 half-tile buffer so far
+      for (int i = 0; i < n_ctx && ok; ++i) {
+        int valid;
+        const int page = tile_pages(i, valid, false);
+        const bool whole = valid == kT && __ballot_sync(0xffffffffu, lane < 8 && page >= 0) == 0xffu;
+        for (int h = 0; h < 2; ++h, ++uses) {
+          const uint32_t slot_full = bar(is_k ? K8_FULL0 + h : V8_FULL0 + h);
+          const uint32_t buf_empty = bar(is_k ? K_EMPTY : V_EMPTY0);
+          if (lane == 0)
+            ok = mbar_wait(slot_full, (uint32_t)(i & 1), sm, p.dev_status) &&
+                 mbar_wait(buf_empty, (uint32_t)(uses & 1) ^ 1u, sm, p.dev_status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const uint32_t src_base = smem_u32((is_k ? sK8 : sV8) + h * kSlotB) + src0;
+          // rows of this lane that hold codes (all of them for a whole tile)
+          uint32_t live = 0xffffu;
+          if (!whole) {
+            live = 0u;
+            for (int u = 0; u < 16; ++u) {
+              const int r = r0 + (is_k ? 8 : 4) * u;
+              const int pg = __shfl_sync(0xffffffffu, page, is_k ? r >> 4 : 4 * h + (r >> 4));
+              const int tok = is_k ? r : 64 * h + r;
+              live |= (pg >= 0 && tok < valid ? 1u : 0u) << u;
+            }
+          }
+#pragma unroll
+          for (int u0 = 0; u0 < 16; u0 += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t a = src_base + (uint32_t)(u0 + k) * 1024u;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                           : "r"(a));
+              if (!((live >> (u0 + k)) & 1u)) v[k] = make_uint4(0, 0, 0, 0);   // past the context / no page
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int u = u0 + k;
+              // the chunk stored first: codes 8-15 (odd chunk) or 0-7
+              const uint32_t f0 = odd_first ? v[k].z : v[k].x, f1 = odd_first ? v[k].w : v[k].y;
+              const uint32_t s0 = odd_first ? v[k].x : v[k].z, s1 = odd_first ? v[k].y : v[k].w;
+              uint4 a, b2;
+              e4m3x4_to_f16x4(f0, a.x, a.y);
+              e4m3x4_to_f16x4(f1, a.z, a.w);
+              e4m3x4_to_f16x4(s0, b2.x, b2.y);
+              e4m3x4_to_f16x4(s1, b2.z, b2.w);
+              const uint32_t grp = is_k ? (uint32_t)u * (kGroupB / 2) : (uint32_t)(u >> 1) * kGroupB;
+              const uint32_t o1 = dst_base + grp + ((u & 1) ? d1o : d1e);
+              const uint32_t o2 = dst_base + grp + ((u & 1) ? d2o : d2e);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(o1), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w)
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(o2), "r"(b2.x), "r"(b2.y), "r"(b2.z),
+                           "r"(b2.w)
+                           : "memory");
+            }
+          }
+          fence_async_smem();   // plain stores, read by the tensor core
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(is_k ? K_FULL : V_FULL0));
+            mbar_arrive(bar(is_k ? K8_EMPTY0 + h : V8_EMPTY0 + h));
+          }
+        }
+        if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
+      }
     }
   } else if (!KV8 && producer) {
     // ------------------------------------------------------------ TMA producers (K or V)
@@ -670,6 +785,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
       int kf = 0, pf = 0, vf0 = 0, vf1 = 0;
       int pv_half = 0;   // the PV product of a context tile runs in two 64-token halves
+      int qk_half = 0;   // quantised cache: the QK product of a context tile runs in two 128-dim halves
       int sfree[2] = {0, 0};
       int qk_next = 0, pv_next = 0;
       long long idle_since = clock64();
@@ -678,27 +794,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         // QK of the next tile: K tile landed, S^T buffer released by the softmax
         if (qk_next < n_tiles && qk_next <= pv_next + 1) {
           const int i = qk_next, sb = i & 1;
-          // (a quantised K tile arrives in two halves of the head dimension)
-          const bool k_ok = (has_draft && i == 0) ||
-                            (mbar_test(bar(K_FULL), kf & 1) && (!KV8 || mbar_test(bar(K_FULL1), kf & 1)));
-          const bool s_ok = i < 2 || mbar_test(bar(S_FREE0 + sb), sfree[sb] & 1);
+          const bool draft_qk = has_draft && i == 0;
+          const bool k_ok = draft_qk || mbar_test(bar(K_FULL), kf & 1);
+          const bool s_ok = qk_half == 1 || i < 2 || mbar_test(bar(S_FREE0 + sb), sfree[sb] & 1);
           if (k_ok && s_ok) {
-            if (!(has_draft && i == 0)) ++kf;
-            if (i >= 2) ++sfree[sb];
+            if (!draft_qk) ++kf;
+            if (qk_half == 0 && i >= 2) ++sfree[sb];
             tc_fence_after();
+            if (KV8 && !draft_qk) {
+              // quantised cache: one 128-dim half from the f16 half-tile buffer (8-row groups 2 KB apart)
 #pragma unroll
-            for (int kk = 0; kk < kDim / 16; ++kk) {
-              // A = K, K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
-              // B = Q^T, K-major, block-major: 64-dim blocks NQ * 128 B apart, 8-row groups 1 KB apart
-              const uint32_t off = (kk & 3) * 32;
-              umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * 1024 + off, 16, kGroupB),
-                   sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024),
-                   kIdescQK, kk > 0 ? 1u : 0u);
-              if (KV8 && kk == kDim / 32 - 1) umma_commit(bar(K_EMPTY));   // dims 0-127 read
+              for (int k8 = 0; k8 < kDim / 32; ++k8) {
+                const int kk = (kDim / 32) * qk_half + k8;
+                const uint32_t off = (k8 & 3) * 32;
+                umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (k8 >> 2) * 1024 + off, 16, kGroupB / 2),
+                     sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(K_EMPTY));
+              if (qk_half == 1) {
+                umma_commit(bar(S_FULL0 + sb));
+                ++qk_next;
+              }
+              qk_half ^= 1;
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < kDim / 16; ++kk) {
+                // A = K, K-major: 64-dim blocks 1 KB apart, 32 bytes per 16-element step, 8-row groups 4 KB apart
+                // B = Q^T, K-major, block-major: 64-dim blocks NQ * 128 B apart, 8-row groups 1 KB apart
+                const uint32_t off = (kk & 3) * 32;
+                umma(tmem + kColS0 + sb * NQ, sw128_desc(k_addr + (kk >> 2) * 1024 + off, 16, kGroupB),
+                     sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024),
+                     kIdescQK, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(S_FULL0 + sb));
+              umma_commit(bar(K_EMPTY));
+              ++qk_next;
             }
-            umma_commit(bar(S_FULL0 + sb));
-            umma_commit(bar(KV8 ? K_EMPTY1 : K_EMPTY));
-            ++qk_next;
             progressed = true;
           }
         }
@@ -706,18 +837,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (pv_next < qk_next) {
           const int t = pv_next;
           const bool draft = has_draft && t == 0;
+          // (quantised cache: both halves pass through the one f16 half-tile buffer of V_FULL0)
           const bool ready = pv_half == 0 ? mbar_test(bar(P_FULL), pf & 1) && (draft || mbar_test(bar(V_FULL0), vf0 & 1))
-                                          : mbar_test(bar(V_FULL1), vf1 & 1);
+                                          : (KV8 ? mbar_test(bar(V_FULL0), vf0 & 1) : mbar_test(bar(V_FULL1), vf1 & 1));
           if (ready) {
             if (pv_half == 0) {
               ++pf;
               if (!draft) ++vf0;
+            } else if (KV8) {
+              ++vf0;
             } else {
               ++vf1;
             }
             tc_fence_after();
-            // O^T += V^T . P^T over 16-token steps j0 .. j0 + steps - 1
-            auto issue_pv = [&](const int j0, const int steps) {
+            // O^T += V^T . P^T over 16-token steps j0 .. j0 + steps - 1 (V rows from step vj0 of the buffer on)
+            auto issue_pv = [&](const int j0, const int steps, const int vj0) {
 #pragma unroll
               for (int jj = 0; jj < steps; ++jj) {
                 const int j = j0 + jj;
@@ -727,23 +861,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
-                  umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + j * 2 * kGroupB, 1024, kGroupB),
+                  umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + (j - vj0) * 2 * kGroupB, 1024, kGroupB),
                        pb, kIdescPV, acc);
                 }
               }
             };
             if (draft) {
               // the draft tile holds n_nodes <= 64 token rows: all in the first half
-              issue_pv(0, (n_nodes + 15) >> 4);
+              issue_pv(0, (n_nodes + 15) >> 4, 0);
               umma_commit(bar(O_DONE));
               ++pv_next;
             } else if (pv_half == 0) {
-              issue_pv(0, kT / 32);
+              issue_pv(0, kT / 32, 0);
               umma_commit(bar(V_EMPTY0));
               pv_half = 1;
             } else {
-              issue_pv(kT / 32, kT / 32);
-              umma_commit(bar(V_EMPTY1));
+              issue_pv(kT / 32, kT / 32, KV8 ? kT / 32 : 0);   // quantised cache: the half-tile buffer
+              umma_commit(bar(KV8 ? V_EMPTY0 : V_EMPTY1));
               umma_commit(bar(O_DONE));
               pv_half = 0;
               ++pv_next;
@@ -1121,6 +1255,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
 }
 
+
+// ---------------------------------------------------------------- host side
+
+// The driver's tensor-map encoder, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
 
 template <int NQ, bool WIN, bool KV8>
 cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, const BatchDesc& bd,
