@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "../../include/sd_gdn.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -99,6 +100,29 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // A per-tensor scale of an e4m3 cache: positive, finite, with a finite fp32 reciprocal.
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && std::isfinite(1.0f / s); }
+
+sd_status check_gdn_shape(const sd_gdn_shape* s, BatchDesc* bd) {
+  if (s == nullptr) return SD_ERR_INVALID_ARG;
+  if (s->head_dim != kGdnDim) return SD_ERR_UNSUPPORTED;
+  if (s->num_k_heads < 1 || s->num_v_heads < s->num_k_heads || s->num_v_heads % s->num_k_heads != 0)
+    return SD_ERR_INVALID_ARG;
+  if (s->num_v_heads > 256) return SD_ERR_UNSUPPORTED;
+  return fill_batch(s->batch, s->q_indptr_h, bd);
+}
+
+// Tree cache of one layer: u [sumN][H_v][128], log decay [sumN][H_v], normalised keys [sumN][H_k][128] (fp32).
+struct GdnCacheLayout {
+  size_t u, g, k, total;
+};
+GdnCacheLayout gdn_cache_layout(const sd_gdn_shape* s, const BatchDesc& bd) {
+  GdnCacheLayout l;
+  const size_t n = (size_t)bd.total_nodes;
+  l.u = 0;
+  l.g = align_up(n * s->num_v_heads * kGdnDim * sizeof(float));
+  l.k = l.g + align_up(n * s->num_v_heads * sizeof(float));
+  l.total = l.k + align_up(n * s->num_k_heads * kGdnDim * sizeof(float));
+  return l;
+}
 
 // sd_verify_attn and sd_verify_attn_fp8: checks, split plan, parameter block, launch.
 sd_status verify_attn(const sd_shape* shape, const void* q, const void* k_cache, const void* v_cache,
@@ -286,6 +310,99 @@ sd_status sd_kv_commit_fp8(const sd_shape* shape, int num_layers, void* const* k
   return kv_commit(shape, num_layers, k_cache_layers, v_cache_layers, k_scales, v_scales, k_new_layers,
                    v_new_layers, page_table, ctx_lens, new_ctx_lens, accept_len, path, max_path, dev_status, stream,
                    true);
+}
+
+size_t sd_gdn_tree_cache_size(const sd_gdn_shape* shape) {
+  BatchDesc bd;
+  if (check_gdn_shape(shape, &bd) != SD_OK) return 0;
+  return gdn_cache_layout(shape, bd).total;
+}
+
+sd_status sd_gdn_conv_tree(int batch, const int* q_indptr_h, int channels, const void* x, const float* weight,
+                           const void* conv_state, const int* parents, void* y, int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = fill_batch(batch, q_indptr_h, &bd);
+  if (st != SD_OK) return st;
+  if (channels < 1 || !x || !weight || !conv_state || !parents || !y) return SD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(y)) return SD_ERR_INVALID_ARG;
+  ConvTreeParams p;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.weight = weight;
+  p.conv_state = static_cast<const __nv_bfloat16*>(conv_state);
+  p.parents = parents;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  p.channels = channels;
+  return cuda_status(launch_conv_tree(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
+sd_status sd_gdn_tree(const sd_gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const float* state, const int* parents, void* out, void* tree_cache,
+                      size_t cache_bytes, int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = check_gdn_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (!q || !k || !v || !g || !beta || !state || !parents || !out) return SD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(out))
+    return SD_ERR_INVALID_ARG;
+  const GdnCacheLayout l = gdn_cache_layout(shape, bd);
+  if (tree_cache == nullptr || cache_bytes < l.total || !aligned16(tree_cache)) return SD_ERR_WORKSPACE;
+  GdnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.state = state;
+  p.parents = parents;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  char* c = static_cast<char*>(tree_cache);
+  p.cache_u = reinterpret_cast<float*>(c + l.u);
+  p.cache_g = reinterpret_cast<float*>(c + l.g);
+  p.cache_k = reinterpret_cast<float*>(c + l.k);
+  p.dev_status = dev_status;
+  p.hk = shape->num_k_heads;
+  p.hv = shape->num_v_heads;
+  return cuda_status(launch_gdn_tree(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
+sd_status sd_gdn_commit(const sd_gdn_shape* shape, int num_layers, float* const* state_layers,
+                        const void* const* tree_cache_layers, int channels, void* const* conv_state_layers,
+                        const void* const* x_layers, const int* accept_len, const int* path, int max_path,
+                        int* dev_status, void* stream) {
+  BatchDesc bd;
+  sd_status st = check_gdn_shape(shape, &bd);
+  if (st != SD_OK) return st;
+  if (num_layers < 1 || channels < 0 || max_path < 1 || !state_layers || !tree_cache_layers || !accept_len || !path)
+    return SD_ERR_INVALID_ARG;
+  if (num_layers > kMaxLayers) return SD_ERR_UNSUPPORTED;
+  if (channels > 0 && (!conv_state_layers || !x_layers)) return SD_ERR_INVALID_ARG;
+  const GdnCacheLayout l = gdn_cache_layout(shape, bd);
+  GdnCommitParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < num_layers; ++i) {
+    if (!state_layers[i] || !tree_cache_layers[i] || !aligned16(state_layers[i]) || !aligned16(tree_cache_layers[i]))
+      return SD_ERR_INVALID_ARG;
+    const char* c = static_cast<const char*>(tree_cache_layers[i]);
+    p.state[i] = state_layers[i];
+    p.cache_u[i] = reinterpret_cast<const float*>(c + l.u);
+    p.cache_g[i] = reinterpret_cast<const float*>(c + l.g);
+    p.cache_k[i] = reinterpret_cast<const float*>(c + l.k);
+    if (channels > 0) {
+      if (!conv_state_layers[i] || !x_layers[i]) return SD_ERR_INVALID_ARG;
+      p.conv_state[i] = static_cast<__nv_bfloat16*>(conv_state_layers[i]);
+      p.x[i] = static_cast<const __nv_bfloat16*>(x_layers[i]);
+    }
+  }
+  p.accept_len = accept_len;
+  p.path = path;
+  p.dev_status = dev_status;
+  p.max_path = max_path;
+  p.num_layers = num_layers;
+  p.hk = shape->num_k_heads;
+  p.hv = shape->num_v_heads;
+  p.channels = channels;
+  return cuda_status(launch_gdn_commit(p, bd, static_cast<cudaStream_t>(stream)));
 }
 
 size_t sd_ddtree_workspace_size(int batch, int positions, int vocab, int topk) {

@@ -44,10 +44,10 @@
 // decode(code) * scale (the quantised KV cache of «如何在单张 RTX 3090 上让
 // Qwen3.5-27B token 生成速度提升 6 倍», 24 GB 显存上的 128K 上下文, here in e4m3).
 // The tensor core takes f16 operands (every e4m3 value is exact in f16), so
-// each tile passes through two stages: a loader warp (9) brings e4m3 half
+// each tile passes through two stages: a loader warp (8) brings e4m3 half
 // tiles by TMA into two 16 KB staging slots per tensor (K: dims 0-127 or
 // 128-255 of every token, one 2 KB box per page; V: pages 0-3 or 4-7, one
-// 4 KB bulk copy per page), and converter warps (0 and 7 for K, 6 and 8 for
+// 4 KB bulk copy per page), and converter warps (0 and 7 for K, 6 and 9 for
 // V) widen a slot into the tensor's single f16 half-tile buffer, which the
 // MMA consumes half by half (QK in two 128-dim steps, PV in two 64-token
 // steps).  A slot is refilled as soon as it has been widened, so the next
@@ -76,7 +76,9 @@ constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 1
 constexpr int kThreads = 224;
 constexpr int kThreads8 = 320;          // the quantised-cache instances: two more converters and a loader
 constexpr int kWarpK = 0, kWarpMma = 1, kWarpV = 6;
-constexpr int kWarpK2 = 7, kWarpV2 = 8, kWarpLoad = 9;   // quantised cache: second K / V converter, TMA loader
+// quantised cache: second K / V converter and the TMA loader, placed so that each of the four
+// schedulers (warp % 4) runs one converter warp
+constexpr int kWarpK2 = 7, kWarpV2 = 9, kWarpLoad = 8;
 constexpr int kHalfB = kTileB / 2;      // quantised cache: f16 half tile (128 tokens x 128 dims, or 64 x 256)
 constexpr int kSlotB = kTileB / 4;      // quantised cache: e4m3 half tile (staging slot)
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling

@@ -80,4 +80,47 @@ struct DdtreeParams {
 size_t ddtree_smem_bytes(int chunks);
 cudaError_t launch_ddtree(const DdtreeParams& p, cudaStream_t st);
 
+// Tree Gated DeltaNet (hybrid layers): tree convolution, gated delta rule over the tree, persist-on-accept.
+constexpr int kGdnDim = 128;       // d_k = d_v
+struct GdnParams {
+  const __nv_bfloat16* q;    // [sumN][hk][128]
+  const __nv_bfloat16* k;    // [sumN][hk][128]
+  const __nv_bfloat16* v;    // [sumN][hv][128]
+  const float* g;            // [sumN][hv] log decay
+  const float* beta;         // [sumN][hv]
+  const float* state;        // [B][hv][128 rows][128]
+  const int* parents;
+  __nv_bfloat16* out;        // [sumN][hv][128]
+  float* cache_u;            // [sumN][hv][128]
+  float* cache_g;            // [sumN][hv] log of the path's decay product
+  float* cache_k;            // [sumN][hk][128] normalised keys
+  int* dev_status;
+  int hk, hv;
+};
+struct GdnCommitParams {
+  float* state[kMaxLayers];
+  const float* cache_u[kMaxLayers];
+  const float* cache_g[kMaxLayers];
+  const float* cache_k[kMaxLayers];
+  __nv_bfloat16* conv_state[kMaxLayers];   // [B][channels][3]
+  const __nv_bfloat16* x[kMaxLayers];      // [sumN][channels]
+  const int* accept_len;
+  const int* path;
+  int* dev_status;
+  int max_path, num_layers, hk, hv, channels;
+};
+struct ConvTreeParams {
+  const __nv_bfloat16* x;           // [sumN][channels]
+  const float* weight;              // [channels][4]
+  const __nv_bfloat16* conv_state;  // [B][channels][3], oldest first
+  const int* parents;
+  __nv_bfloat16* y;                 // [sumN][channels]
+  int* dev_status;
+  int channels;
+};
+size_t gdn_smem_bytes(int max_nodes);
+cudaError_t launch_gdn_tree(const GdnParams& p, const BatchDesc& bd, cudaStream_t st);
+cudaError_t launch_gdn_commit(const GdnCommitParams& p, const BatchDesc& bd, cudaStream_t st);
+cudaError_t launch_conv_tree(const ConvTreeParams& p, const BatchDesc& bd, cudaStream_t st);
+
 }  // namespace sdv

@@ -39,6 +39,11 @@ class SdShape(ctypes.Structure):
                 ("window", ctypes.c_int)]
 
 
+class SdGdnShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("q_indptr_h", ctypes.POINTER(ctypes.c_int)),
+                ("num_k_heads", ctypes.c_int), ("num_v_heads", ctypes.c_int), ("head_dim", ctypes.c_int)]
+
+
 class SdError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -82,6 +87,15 @@ def load() -> ctypes.CDLL:
     fpp = ctypes.POINTER(ctypes.c_float)
     lib.sd_kv_commit_fp8.argtypes = [shp, ctypes.c_int, pp, pp, fpp, fpp, pp, pp, vp, vp, vp, vp, vp, ctypes.c_int,
                                      vp, vp]
+    gshp = ctypes.POINTER(SdGdnShape)
+    lib.sd_gdn_tree_cache_size.restype = sz
+    lib.sd_gdn_tree_cache_size.argtypes = [gshp]
+    lib.sd_gdn_conv_tree.restype = ctypes.c_int
+    lib.sd_gdn_conv_tree.argtypes = [ctypes.c_int, ip, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp]
+    lib.sd_gdn_tree.restype = ctypes.c_int
+    lib.sd_gdn_tree.argtypes = [gshp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.sd_gdn_commit.restype = ctypes.c_int
+    lib.sd_gdn_commit.argtypes = [gshp, ctypes.c_int, pp, pp, ctypes.c_int, pp, pp, vp, vp, ctypes.c_int, vp, vp]
     lib.sd_ddtree_workspace_size.restype = sz
     lib.sd_ddtree_workspace_size.argtypes = [ctypes.c_int] * 4
     lib.sd_ddtree_build.restype = ctypes.c_int
@@ -242,3 +256,56 @@ def sd_ddtree_build(draft_logits, topk: int, budget: int, root_tokens, parents, 
                                   _ptr(root_tokens), _ptr(parents), _ptr(tokens), _ptr(scores), _ptr(workspace),
                                   ws_bytes, _ptr(dev_status), _stream(stream)),
            "sd_ddtree_build")
+
+
+class GdnShape:
+    """An sd_gdn_shape with its host q_indptr kept alive (head_dim 128)."""
+
+    def __init__(self, q_indptr, num_k_heads: int, num_v_heads: int, head_dim: int = 128):
+        self.indptr = _indptr(q_indptr)
+        self.c = SdGdnShape(len(self.indptr) - 1, ctypes.cast(self.indptr, ctypes.POINTER(ctypes.c_int)),
+                            int(num_k_heads), int(num_v_heads), int(head_dim))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def sd_gdn_tree_cache_size(shape: GdnShape) -> int:
+    return int(load().sd_gdn_tree_cache_size(shape.ref))
+
+
+def sd_gdn_conv_tree(q_indptr, x, weight, conv_state, parents, y, dev_status=None, stream=None) -> None:
+    """x, y bf16 [sumN, C]; weight fp32 [C, 4]; conv_state bf16 [B, C, 3]."""
+    ind = _indptr(q_indptr)
+    _check(load().sd_gdn_conv_tree(len(ind) - 1, ind, int(x.shape[-1]), _ptr(x), _ptr(weight), _ptr(conv_state),
+                                   _ptr(parents), _ptr(y), _ptr(dev_status), _stream(stream)),
+           "sd_gdn_conv_tree")
+
+
+def sd_gdn_tree(shape: GdnShape, q, k, v, g, beta, state, parents, out, tree_cache, dev_status=None,
+                stream=None) -> None:
+    cache_bytes = tree_cache.numel() * tree_cache.element_size()
+    _check(load().sd_gdn_tree(shape.ref, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(parents),
+                              _ptr(out), _ptr(tree_cache), cache_bytes, _ptr(dev_status), _stream(stream)),
+           "sd_gdn_tree")
+
+
+def sd_gdn_commit(shape: GdnShape, state_layers, tree_cache_layers, accept_len, path, conv_state_layers=None,
+                  x_layers=None, max_path: int | None = None, dev_status=None, stream=None) -> None:
+    n = len(state_layers)
+    if len(tree_cache_layers) != n:
+        raise ValueError("per-layer lists differ in length")
+    channels = 0
+    conv_arr = x_arr = None
+    if conv_state_layers is not None:
+        if len(conv_state_layers) != n or x_layers is None or len(x_layers) != n:
+            raise ValueError("per-layer lists differ in length")
+        channels = int(x_layers[0].shape[-1])
+        conv_arr, x_arr = _ptr_array(conv_state_layers), _ptr_array(x_layers)
+    if max_path is None:
+        max_path = path.shape[-1]
+    _check(load().sd_gdn_commit(shape.ref, n, _ptr_array(state_layers), _ptr_array(tree_cache_layers), channels,
+                                conv_arr, x_arr, _ptr(accept_len), _ptr(path), int(max_path), _ptr(dev_status),
+                                _stream(stream)),
+           "sd_gdn_commit")

@@ -348,3 +348,38 @@ def draft_logits(batch: int, positions: int, vocab: int, seed: int, scale: float
     if ties:
         x = np.round(x * 4.0) / 4.0
     return x
+
+
+# Gated DeltaNet layers of the hybrid model: 16 key heads, 32 value heads, head dim 128 (a reading: the
+# pages name the layer type only); the short convolution runs over the q, k and v channels.
+GDN_HK, GDN_HV, GDN_D = 16, 32, 128
+GDN_CHANNELS = 2 * GDN_HK * GDN_D + GDN_HV * GDN_D
+
+
+@dataclass
+class GdnInputs:
+    """One Gated DeltaNet layer's verify inputs for a batch of draft trees (device tensors)."""
+
+    q: torch.Tensor            # bf16 [sumN, H_k, 128]
+    k: torch.Tensor            # bf16 [sumN, H_k, 128]
+    v: torch.Tensor            # bf16 [sumN, H_v, 128]
+    g: torch.Tensor            # fp32 [sumN, H_v] log decay (<= 0)
+    beta: torch.Tensor         # fp32 [sumN, H_v] in [0, 1]
+    state: torch.Tensor        # fp32 [B, H_v, 128, 128]
+    x: torch.Tensor            # bf16 [sumN, C] convolution inputs
+    conv_w: torch.Tensor       # fp32 [C, 4]
+    conv_state: torch.Tensor   # bf16 [B, C, 3]
+
+
+def gdn_inputs(n_total: int, batch: int, seed: int, device="cpu", hk: int = GDN_HK, hv: int = GDN_HV,
+               channels: int = GDN_CHANNELS, state_scale: float = 0.05, decay: float = 0.5) -> GdnInputs:
+    """Seeded draws: q, k, v, x ~ N(0, 1) (bf16); g ~ -U(0, decay); beta ~ U(0, 1); state ~ N(0, state_scale^2);
+    convolution taps ~ N(0, 0.5^2); convolution state ~ N(0, 1) (bf16)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) * 7907 + 11)
+    rn = lambda *shape: torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    ru = lambda *shape: torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+    return GdnInputs(q=rn(n_total, hk, GDN_D).to(torch.bfloat16), k=rn(n_total, hk, GDN_D).to(torch.bfloat16),
+                     v=rn(n_total, hv, GDN_D).to(torch.bfloat16), g=-decay * ru(n_total, hv), beta=ru(n_total, hv),
+                     state=state_scale * rn(batch, hv, GDN_D, GDN_D), x=rn(n_total, channels).to(torch.bfloat16),
+                     conv_w=0.5 * rn(channels, 4), conv_state=rn(batch, channels, 3).to(torch.bfloat16))

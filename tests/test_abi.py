@@ -13,7 +13,8 @@ import pytest
 
 from speculative_decoding_verify_decode_gb300 import build, native
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sd_verify.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = [os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h")]
 FAKE = 0x10000   # never dereferenced: each call returns before launching
 
 
@@ -24,8 +25,11 @@ def lib():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    names = set(re.findall(r"\b(sd_[a-z_]+)\s*\(", open(HEADER).read()))
-    assert {"sd_verify_attn", "sd_accept", "sd_kv_commit", "sd_status_string"} <= names
+    names = set()
+    for h in HEADERS:
+        names |= set(re.findall(r"\b(sd_[a-z0-9_]+)\s*\(", open(h).read()))
+    assert {"sd_verify_attn", "sd_accept", "sd_kv_commit", "sd_status_string", "sd_verify_attn_fp8",
+            "sd_kv_commit_fp8", "sd_gdn_tree", "sd_gdn_commit", "sd_gdn_conv_tree"} <= names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -152,3 +156,30 @@ def test_fp8_scales_checked_before_any_launch(lib):
     assert commit(None, good) == native.SD_ERR_INVALID_ARG
     assert commit(good, bad) == native.SD_ERR_INVALID_ARG
     assert commit(bad, good) == native.SD_ERR_INVALID_ARG
+
+
+
+def test_gdn_host_checks(lib):
+    ind = [0, 23]
+    ok = native.GdnShape(ind, 16, 32)
+    assert lib.sd_gdn_tree_cache_size(ok.ref) == 23 * 32 * 128 * 4 + 3072 + 23 * 16 * 128 * 4
+    assert lib.sd_gdn_tree_cache_size(native.GdnShape(ind, 16, 32, head_dim=64).ref) == 0
+    assert lib.sd_gdn_tree_cache_size(native.GdnShape(ind, 16, 24).ref) == 0      # H_v not a multiple of H_k
+    call = lambda s, cache=FAKE, nbytes=1 << 30, q=FAKE: lib.sd_gdn_tree(s.ref, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                                        FAKE, cache, nbytes, None, None)
+    assert call(native.GdnShape(ind, 16, 32, head_dim=256)) == native.SD_ERR_UNSUPPORTED
+    assert call(native.GdnShape(ind, 16, 512)) == native.SD_ERR_UNSUPPORTED
+    assert call(native.GdnShape(ind, 0, 32)) == native.SD_ERR_INVALID_ARG
+    assert call(ok, q=None) == native.SD_ERR_INVALID_ARG
+    assert call(ok, q=FAKE + 2) == native.SD_ERR_INVALID_ARG
+    assert call(ok, cache=None) == native.SD_ERR_WORKSPACE
+    assert call(ok, nbytes=16) == native.SD_ERR_WORKSPACE
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    commit = lambda layers, ch=0, conv=None: lib.sd_gdn_commit(ok.ref, layers, arr, arr, ch, conv, conv, FAKE, FAKE,
+                                                               8, None, None)
+    assert commit(0) == native.SD_ERR_INVALID_ARG
+    assert commit(native.MAX_LAYERS + 1) == native.SD_ERR_UNSUPPORTED
+    assert commit(2, ch=8192, conv=None) == native.SD_ERR_INVALID_ARG
+    ind2 = (ctypes.c_int * 2)(0, 23)
+    assert lib.sd_gdn_conv_tree(1, ind2, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == native.SD_ERR_INVALID_ARG
+    assert lib.sd_gdn_conv_tree(1, ind2, 64, None, FAKE, FAKE, FAKE, FAKE, None, None) == native.SD_ERR_INVALID_ARG
