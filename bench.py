@@ -195,6 +195,98 @@ def time_ddtree_build(dev, stream, batch: int, budget: int, positions: int = 16,
             "shape": {"batch": batch, "positions": positions, "vocab": vocab, "topk": topk, "budget": budget}}
 
 
+GDN_LAYERS = 48    # Gated DeltaNet layers of the hybrid model (48 of 64)
+
+
+def gdn_bytes_per_layer(batch: int, n_total: int) -> dict:
+    """Algorithmic bytes of one Gated DeltaNet layer's tree verify and of its commit.
+
+    Tree rule: the cached state (H_v x 128 x 128 fp32 = 64 KB per value head) is read once per sequence;
+    q and k (H_k x 128 bf16), v and o (H_v x 128 bf16), g and beta (fp32) per node; the tree cache it
+    writes (u: H_v x 128 fp32, normalised keys: H_k x 128 fp32, log decays).  Convolution: x and y
+    (C bf16) per node, the taps (C x 4 fp32) and the convolution state (C x 3 bf16) per sequence.
+    Commit: the state is read and written once; the path's cache rows are read.
+    """
+    hk, hv, d, c = synth.GDN_HK, synth.GDN_HV, synth.GDN_D, synth.GDN_CHANNELS
+    state = batch * hv * d * d * 4
+    tree = state + n_total * (2 * hk * d * 2 + 2 * hv * d * 2 + hv * 8 + hv * d * 4 + hk * d * 4 + hv * 4)
+    conv = n_total * c * 4 + c * 16 + batch * c * 6
+    return {"tree": tree, "conv": conv, "commit": 2 * state}
+
+
+def time_gdn(dev, stream, w, reps: int) -> dict:
+    """The hybrid layers' verify for the workload's draft trees: per layer the tree convolution and the tree
+    gated delta rule (48 layers in one CUDA graph), then persist-on-accept of all 48 layers in one launch."""
+    n, B = w.total_nodes, w.batch
+    parents = torch.as_tensor(w.parents, dtype=torch.int32, device=dev)
+    shape = native.GdnShape(w.q_indptr, synth.GDN_HK, synth.GDN_HV)
+    ins = [synth.gdn_inputs(n, B, 100 + layer, device=dev) for layer in range(GDN_LAYERS)]
+    caches = [torch.empty(native.sd_gdn_tree_cache_size(shape), dtype=torch.uint8, device=dev) for _ in ins]
+    outs = [torch.empty_like(x.v) for x in ins]
+    ys = [torch.empty_like(x.x) for x in ins]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # a valid accept result: every sequence keeps its root only (A = 1)
+    lens = torch.ones(B, dtype=torch.int32, device=dev)
+    path = torch.zeros((B, 1), dtype=torch.int32, device=dev)
+
+    def layers(s):
+        for x, cache, out, y in zip(ins, caches, outs, ys):
+            native.sd_gdn_conv_tree(w.q_indptr, x.x, x.conv_w, x.conv_state, parents, y, status, stream=s)
+            native.sd_gdn_tree(shape, x.q, x.k, x.v, x.g, x.beta, x.state, parents, out, cache, status, stream=s)
+
+    def commit(s):
+        native.sd_gdn_commit(shape, [x.state for x in ins], caches, lens, path,
+                             conv_state_layers=[x.conv_state for x in ins], x_layers=[x.x for x in ins],
+                             dev_status=status, stream=s)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                fn(cap)
+        stream.wait_stream(cap)
+        return g
+
+    g_layers, g_commit = graph_of(layers), graph_of(commit)
+    res = {}
+    for name, g in (("layers", g_layers), ("commit", g_commit)):
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) * 1000.0 / reps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the hybrid layers")
+    # the tree rule alone (the dominant kernel of the hybrid layers)
+    g_tree = graph_of(lambda s: [native.sd_gdn_tree(shape, x.q, x.k, x.v, x.g, x.beta, x.state, parents, out, cache,
+                                                    status, stream=s) for x, cache, out in zip(ins, caches, outs)])
+    for _ in range(3):
+        g_tree.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g_tree.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    tree_us = e0.elapsed_time(e1) * 1000.0 / (reps * GDN_LAYERS)
+    by = gdn_bytes_per_layer(B, n)
+    peak, _ = peaks()
+    tree_gbs = by["tree"] / (tree_us * 1e-6) / 1e9
+    commit_gbs = GDN_LAYERS * by["commit"] / (res["commit"] * 1e-6) / 1e9
+    return {"layers": GDN_LAYERS, "heads": f"{synth.GDN_HK}k/{synth.GDN_HV}v", "head_dim": synth.GDN_D,
+            "conv_channels": synth.GDN_CHANNELS, "us_per_step_layers": res["layers"],
+            "us_per_layer": res["layers"] / GDN_LAYERS, "tree_us_per_layer": tree_us,
+            "tree_alg_bytes_per_layer": by["tree"], "tree_gbs": tree_gbs, "tree_frac": tree_gbs / peak,
+            "commit_us": res["commit"], "commit_gbs": commit_gbs, "commit_frac": commit_gbs / peak,
+            "launches_per_step": 2 * GDN_LAYERS + 2}
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -318,6 +410,8 @@ def run_ours(args, world, rank, local):
     }
     if args.config.startswith("ddtree"):
         line["ddtree_build"] = time_ddtree_build(dev, stream, w.batch, w.total_nodes // w.batch - 1)
+    if not args.no_gdn:
+        line["gdn_layers"] = time_gdn(dev, stream, w, reps=max(5, args.steps // 2))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.config, reps=1)
     return line
@@ -396,6 +490,7 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gdn", action="store_true", help="skip the hybrid (Gated DeltaNet) layers' timing")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload to build (0 = its own count; fewer only for profiler captures)")
     ap.add_argument("--splits", type=int, default=0, help="split-KV chunks per (sequence, KV head); 0 = auto")

@@ -31,20 +31,34 @@ namespace sdv {
 namespace {
 
 constexpr int kD = kGdnDim;        // d_k = d_v
-constexpr int kRows = 32;          // state rows per CTA
-constexpr int kPad = kD + 1;       // padded state row in shared memory (no bank conflicts across rows)
+constexpr int kRows = 16;          // state rows per CTA
+constexpr int kLd = kD + 4;        // padded row (state, keys, queries): 8 consecutive rows read as float4 hit
+                                   // 8 distinct 16-byte bank groups
 constexpr int kGdnThreads = 256;
 
-struct GdnSmem {
-  // sizes for n nodes, laid out by gdn_smem_bytes
-  static size_t bytes(int n) {
-    return sizeof(float) * ((size_t)kRows * kPad + 2 * (size_t)n * kD + (size_t)n * kRows * 4 +
-                            2 * (size_t)n * n + 4 * (size_t)n) +
-           sizeof(unsigned long long) * n + sizeof(int) * n;
-  }
-};
+size_t gdn_tree_smem(int n) {
+  return sizeof(float) * ((size_t)kRows * kLd + 2 * (size_t)n * kLd + (size_t)(4 * n + 1) * kRows +
+                          2 * (size_t)n * (n + 1) + 4 * (size_t)n) +
+         (size_t)n * kMaxNodes + sizeof(int) * 2 * (size_t)n;
+}
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 128-element dot product of two padded shared-memory rows (float4 loads, four partial sums).
+__device__ __forceinline__ float dot128(const float* a, const float* b) {
+  const float4* a4 = reinterpret_cast<const float4*>(a);
+  const float4* b4 = reinterpret_cast<const float4*>(b);
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 8
+  for (int t = 0; t < kD / 4; ++t) {
+    const float4 x = a4[t], y = b4[t];
+    s0 = fmaf(x.x, y.x, s0);
+    s1 = fmaf(x.y, y.y, s1);
+    s2 = fmaf(x.z, y.z, s2);
+    s3 = fmaf(x.w, y.w, s3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
 
 __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p, const BatchDesc bd) {
   extern __shared__ __align__(16) float smem[];
@@ -56,141 +70,145 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
   const int n = bd.q_indptr[b + 1] - q0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  float* s0 = smem;                              // [32][kPad]
-  float* kh = s0 + kRows * kPad;                 // [n][128] normalised keys
-  float* qh = kh + n * kD;                       // [n][128] normalised, scaled queries
-  float* vv = qh + n * kD;                       // [n][32] this block's value rows
-  float* W = vv + n * kRows;                     // [n][32] S_0 k_j
-  float* Z = W + n * kRows;                      // [n][32] S_0 q_j
-  float* U = Z + n * kRows;                      // [n][32]
-  float* A = U + n * kRows;                      // [n][n] beta_j e^{G_j - G_m} (k_m . k_j), m above j
-  float* C = A + n * n;                          // [n][n] e^{G_j - G_m} (k_m . q_j), m on j's path
-  float* G = C + n * n;                          // [n] log gamma
-  float* beta = G + n;                           // [n]
-  float* gg = beta + n;                          // [n] g
-  float* pad_ = gg + n;                          // [n] (keeps the 8-byte arrays aligned)
-  unsigned long long* anc = reinterpret_cast<unsigned long long*>(pad_ + n);   // [n] path bits, j included
-  int* par = reinterpret_cast<int*>(anc + n);
+  float* s0 = smem;                              // [16][kLd] this block's state rows
+  float* kh = s0 + kRows * kLd;                  // [n][kLd] normalised keys
+  float* qh = kh + n * kLd;                      // [n][kLd] normalised, scaled queries
+  float* vv = qh + n * kLd;                      // [n][16] this block's value rows
+  float* W = vv + n * kRows;                     // [n][16] S_0 k_j
+  float* Z = W + n * kRows;                      // [n][16] S_0 q_j
+  float* U = Z + n * kRows;                      // [n + 1][16]; row n stays zero (padding of the sums)
+  float* A = U + (n + 1) * kRows;                // [n][n + 1] beta_j e^{G_j - G_m} (k_m . k_j), m above j
+  float* C = A + n * (n + 1);                    // [n][n + 1] e^{G_j - G_m} (k_m . q_j), m on j's path
+  float* G = C + n * (n + 1);                    // [n] log of the path's decay product
+  float* beta = G + n;
+  float* gg = beta + n;
+  float* eg = gg + n;                            // [n] e^{G_j}
+  int* par = reinterpret_cast<int*>(eg + n);     // [n]
+  int* depth = par + n;                          // [n] proper ancestors of j
+  uint8_t* alist = reinterpret_cast<uint8_t*>(depth + n);   // [n][64] proper ancestors, padded with n
 
-  // ---- tree: parents, gates, ancestor sets and log-decays (thread j walks its root path)
-  for (int j = tid; j < n; j += kGdnThreads) {
-    int pj = p.parents[q0 + j];
-    if ((j == 0 && pj != -1) || (j > 0 && (pj < 0 || pj >= j))) {
-      report(p.dev_status, SD_DEV_BAD_PARENTS);
-      pj = j == 0 ? -1 : j - 1;   // a chain stands in for a broken tree (the output is unspecified)
-    }
-    par[j] = pj;
-    gg[j] = p.g[(size_t)(q0 + j) * p.hv + h];
-    beta[j] = p.beta[(size_t)(q0 + j) * p.hv + h];
-  }
-  __syncthreads();
-  for (int j = tid; j < n; j += kGdnThreads) {
-    unsigned long long a = 0ull;
-    float lg = 0.f;
-    for (int u = j; u >= 0; u = par[u]) {
-      a |= 1ull << u;
-      lg += gg[u];
-    }
-    anc[j] = a;
-    G[j] = lg;
-  }
-  // ---- normalised keys and queries of the key head (a warp per node), this block's value rows
-  const float qscale = rsqrtf((float)kD);
-  for (int j = warp; j < n; j += kGdnThreads / 32) {
-    const __nv_bfloat16* kr = p.k + ((size_t)(q0 + j) * p.hk + hk) * kD;
-    const __nv_bfloat16* qr = p.q + ((size_t)(q0 + j) * p.hk + hk) * kD;
-    float kv4[4], qv4[4], sk = 0.f, sq = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kv4[e] = bf2f(kr[lane + 32 * e]);
-      qv4[e] = bf2f(qr[lane + 32 * e]);
-      sk += kv4[e] * kv4[e];
-      sq += qv4[e] * qv4[e];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    }
-    const float ik = sk > 0.f ? rsqrtf(sk) : 0.f, iq = sq > 0.f ? rsqrtf(sq) * qscale : 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kh[j * kD + lane + 32 * e] = kv4[e] * ik;
-      qh[j * kD + lane + 32 * e] = qv4[e] * iq;
-    }
-  }
-  for (int i = tid; i < n * kRows; i += kGdnThreads) {
-    const int j = i / kRows, r = i % kRows;
-    vv[i] = bf2f(p.v[((size_t)(q0 + j) * p.hv + h) * kD + rb * kRows + r]);
-  }
-  // ---- this block's 32 state rows (16 KB contiguous), float4 loads
+  // ---- every global load of the CTA, before any barrier
   {
     const float4* src = reinterpret_cast<const float4*>(p.state + (((size_t)b * p.hv + h) * kD + rb * kRows) * kD);
     for (int i = tid; i < kRows * kD / 4; i += kGdnThreads) {
-      const float4 x = __ldg(src + i);
       const int r = (i * 4) / kD, c = (i * 4) % kD;
-      float* d = s0 + r * kPad + c;
-      d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+      *reinterpret_cast<float4*>(s0 + r * kLd + c) = __ldg(src + i);
     }
-  }
-  __syncthreads();
-  // ---- W[j][r] = S_0[r] . k_j and Z[j][r] = S_0[r] . q_j: lane = row, warps over nodes
-  for (int j = warp; j < n; j += kGdnThreads / 32) {
-    float aw = 0.f, az = 0.f;
-    const float* sr = s0 + lane * kPad;
-#pragma unroll 8
-    for (int c = 0; c < kD; ++c) {
-      const float s = sr[c];
-      aw = fmaf(s, kh[j * kD + c], aw);
-      az = fmaf(s, qh[j * kD + c], az);
+    for (int i = tid; i < n * kRows; i += kGdnThreads) {
+      const int j = i / kRows, r = i % kRows;
+      vv[i] = bf2f(p.v[((size_t)(q0 + j) * p.hv + h) * kD + rb * kRows + r]);
     }
-    W[j * kRows + lane] = aw;
-    Z[j * kRows + lane] = az;
-  }
-  // ---- pair coefficients under the ancestor mask (dot products start at a rotated dim: no conflicts)
-  for (int i = tid; i < n * n; i += kGdnThreads) {
-    const int j = i / n, m = i % n;
-    float a = 0.f, c = 0.f;
-    if ((anc[j] >> m) & 1ull) {
-      float dk = 0.f, dq = 0.f;
-      for (int t = 0; t < kD; ++t) {
-        const int e = (t + i) & (kD - 1);
-        const float km = kh[m * kD + e];
-        dk = fmaf(km, kh[j * kD + e], dk);
-        dq = fmaf(km, qh[j * kD + e], dq);
+    if (tid < kRows) U[n * kRows + tid] = 0.f;
+    for (int j = tid; j < n; j += kGdnThreads) {
+      int pj = p.parents[q0 + j];
+      if ((j == 0 && pj != -1) || (j > 0 && (pj < 0 || pj >= j))) {
+        if (rb == 0 && h == 0) report(p.dev_status, SD_DEV_BAD_PARENTS);
+        pj = j == 0 ? -1 : j - 1;   // a chain stands in for a broken tree (the output is unspecified)
       }
-      const float ratio = __expf(G[j] - G[m]);
-      if (m != j) a = beta[j] * ratio * dk;
-      c = ratio * dq;
+      par[j] = pj;
+      gg[j] = p.g[(size_t)(q0 + j) * p.hv + h];
+      beta[j] = p.beta[(size_t)(q0 + j) * p.hv + h];
     }
-    A[i] = a;
-    C[i] = c;
+    // normalised keys and queries of the key head, a warp per node
+    const float qscale = rsqrtf((float)kD);
+    for (int j = warp; j < n; j += kGdnThreads / 32) {
+      const __nv_bfloat16* kr = p.k + ((size_t)(q0 + j) * p.hk + hk) * kD;
+      const __nv_bfloat16* qr = p.q + ((size_t)(q0 + j) * p.hk + hk) * kD;
+      float kv4[4], qv4[4], sk = 0.f, sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kv4[e] = bf2f(kr[lane + 32 * e]);
+        qv4[e] = bf2f(qr[lane + 32 * e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sk = fmaf(kv4[e], kv4[e], sk);
+        sq = fmaf(qv4[e], qv4[e], sq);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      }
+      const float ik = sk > 0.f ? rsqrtf(sk) : 0.f, iq = sq > 0.f ? rsqrtf(sq) * qscale : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kh[j * kLd + lane + 32 * e] = kv4[e] * ik;
+        qh[j * kLd + lane + 32 * e] = qv4[e] * iq;
+      }
+    }
   }
   __syncthreads();
-  // ---- u in node order (a node's ancestors come first): one warp, lane = row
-  if (warp == 0) {
+  // ---- root paths (thread j): ancestor list, depth, log-decay; S_0 k_j and S_0 q_j (thread = (row, node))
+  for (int j = tid; j < n; j += kGdnThreads) {
+    float lg = gg[j];
+    int d = 0;
+    for (int u = par[j]; u >= 0; u = par[u]) {
+      alist[j * kMaxNodes + d++] = (uint8_t)u;
+      lg += gg[u];
+    }
+    for (int e = d; e < ((d + 3) & ~3); ++e) alist[j * kMaxNodes + e] = (uint8_t)n;   // padding: the zero row
+    depth[j] = d;
+    G[j] = lg;
+    eg[j] = __expf(lg);
+  }
+  {
+    const int r = tid & (kRows - 1);
+    for (int j = tid / kRows; j < n; j += kGdnThreads / kRows) {
+      W[j * kRows + r] = dot128(s0 + r * kLd, kh + j * kLd);
+      Z[j * kRows + r] = dot128(s0 + r * kLd, qh + j * kLd);
+    }
+  }
+  __syncthreads();
+  // ---- pair coefficients along each node's path (row j, column = ancestor index; column n = padding 0)
+  for (int i = tid; i < n * kMaxNodes; i += kGdnThreads) {
+    const int j = i / kMaxNodes, e = i % kMaxNodes;
+    const int d = depth[j];
+    if (e > d) continue;
+    const int m = e < d ? alist[j * kMaxNodes + e] : j;   // the ancestors, then j itself
+    const float ratio = __expf(G[j] - G[m]);
+    if (m != j) A[j * (n + 1) + m] = beta[j] * ratio * dot128(kh + m * kLd, kh + j * kLd);
+    C[j * (n + 1) + m] = ratio * dot128(kh + m * kLd, qh + j * kLd);
+    if (e == 0) {
+      A[j * (n + 1) + n] = 0.f;
+      C[j * (n + 1) + n] = 0.f;
+    }
+  }
+  __syncthreads();
+  // ---- u in node order (a node's ancestors come first): lane = row, four ancestors per round
+  if (warp == 0 && lane < kRows) {
     for (int j = 0; j < n; ++j) {
-      float acc = beta[j] * (vv[j * kRows + lane] - __expf(G[j]) * W[j * kRows + lane]);
-      unsigned long long a = anc[j] & ~(1ull << j);
-      while (a != 0ull) {
-        const int m = __ffsll((long long)a) - 1;
-        a &= a - 1ull;
-        acc = fmaf(-A[j * n + m], U[m * kRows + lane], acc);
+      float acc = beta[j] * (vv[j * kRows + lane] - eg[j] * W[j * kRows + lane]);
+      const uint8_t* al = alist + j * kMaxNodes;
+      const float* aj = A + j * (n + 1);
+      const int d = depth[j];
+      for (int e = 0; e < d; e += 4) {
+        const int m0 = al[e], m1 = al[e + 1], m2 = al[e + 2], m3 = al[e + 3];
+        const float a0 = aj[m0], a1 = aj[m1], a2 = aj[m2], a3 = aj[m3];
+        const float u0 = U[m0 * kRows + lane], u1 = U[m1 * kRows + lane];
+        const float u2 = U[m2 * kRows + lane], u3 = U[m3 * kRows + lane];
+        acc = fmaf(-a0, u0, acc);
+        acc = fmaf(-a1, u1, acc);
+        acc = fmaf(-a2, u2, acc);
+        acc = fmaf(-a3, u3, acc);
       }
       U[j * kRows + lane] = acc;
-      __syncwarp();
     }
   }
   __syncthreads();
   // ---- outputs, u, log-decays and normalised keys
   for (int i = tid; i < n * kRows; i += kGdnThreads) {
     const int j = i / kRows, r = i % kRows;
-    float acc = __expf(G[j]) * Z[j * kRows + r];
-    unsigned long long a = anc[j];
-    while (a != 0ull) {
-      const int m = __ffsll((long long)a) - 1;
-      a &= a - 1ull;
-      acc = fmaf(C[j * n + m], U[m * kRows + r], acc);
+    const float* cj = C + j * (n + 1);
+    const uint8_t* al = alist + j * kMaxNodes;
+    float acc = fmaf(cj[j], U[i], eg[j] * Z[i]);
+    const int d = depth[j];
+    for (int e = 0; e < d; e += 4) {
+      const int m0 = al[e], m1 = al[e + 1], m2 = al[e + 2], m3 = al[e + 3];
+      acc = fmaf(cj[m0], U[m0 * kRows + r], acc);
+      acc = fmaf(cj[m1], U[m1 * kRows + r], acc);
+      acc = fmaf(cj[m2], U[m2 * kRows + r], acc);
+      acc = fmaf(cj[m3], U[m3 * kRows + r], acc);
     }
     const size_t row = (size_t)(q0 + j) * p.hv + h;
     p.out[row * kD + rb * kRows + r] = __float2bfloat16_rn(acc);
@@ -200,7 +218,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
     for (int j = tid; j < n; j += kGdnThreads) p.cache_g[(size_t)(q0 + j) * p.hv + h] = G[j];
   if (rb == 0 && h % (p.hv / p.hk) == 0)
     for (int i = tid; i < n * kD; i += kGdnThreads)
-      p.cache_k[((size_t)(q0 + i / kD) * p.hk + hk) * kD + i % kD] = kh[i];
+      p.cache_k[((size_t)(q0 + i / kD) * p.hk + hk) * kD + i % kD] = kh[(i / kD) * kLd + i % kD];
 }
 
 // Persist-on-accept of the recurrent state, every layer in one launch:
@@ -284,44 +302,54 @@ __global__ void __launch_bounds__(256) conv_commit_kernel(const GdnCommitParams 
 }
 
 // Causal 4-tap depthwise convolution + SiLU along each node's parent chain.
-// Block: 256 channels of one sequence, every node.
+// Block: 256 channels of one node (grid y = node row); the node's sequence
+// is found in the batch's row offsets and its parents are read once into
+// shared memory, so each thread issues its four window loads at once.
 __global__ void __launch_bounds__(256) conv_tree_kernel(const ConvTreeParams p, const BatchDesc bd) {
   __shared__ int par[kMaxNodes];
-  const int b = blockIdx.y;
+  const int row = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  int lo = 0, hi = bd.batch;   // sequence b with q_indptr[b] <= row < q_indptr[b + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (bd.q_indptr[mid] <= row) lo = mid; else hi = mid;
+  }
+  const int b = lo;
   const int q0 = bd.q_indptr[b];
   const int n = bd.q_indptr[b + 1] - q0;
+  const int j = row - q0;
   if (threadIdx.x < n) {
-    const int j = threadIdx.x;
-    int pj = p.parents[q0 + j];
-    if ((j == 0 && pj != -1) || (j > 0 && (pj < 0 || pj >= j))) {
-      if (blockIdx.x == 0) report(p.dev_status, SD_DEV_BAD_PARENTS);
-      pj = j == 0 ? -1 : j - 1;
+    const int t = threadIdx.x;
+    int pt = p.parents[q0 + t];
+    if ((t == 0 && pt != -1) || (t > 0 && (pt < 0 || pt >= t))) {
+      if (blockIdx.x == 0 && t == j) report(p.dev_status, SD_DEV_BAD_PARENTS);
+      pt = t == 0 ? -1 : t - 1;
     }
-    par[j] = pj;
+    par[t] = pt;
   }
   __syncthreads();
   if (c >= p.channels) return;
+  // window, newest first: the node, its parent, ... then the cached inputs (newest first)
+  int src[4];
+  int u = j, t = 0;
+  for (; t < 4 && u >= 0; ++t, u = par[u]) src[t] = u;
+  const int on_tree = t;
   const float4 w = reinterpret_cast<const float4*>(p.weight)[c];   // w.w multiplies the node's own input
   const __nv_bfloat16* cs = p.conv_state + ((size_t)b * p.channels + c) * 3;
-  const float s0 = bf2f(cs[0]), s1 = bf2f(cs[1]), s2 = bf2f(cs[2]);
-  for (int j = 0; j < n; ++j) {
-    float x[4];   // newest first
-    int u = j, t = 0;
-    for (; t < 4 && u >= 0; ++t, u = par[u]) x[t] = bf2f(p.x[(size_t)(q0 + u) * p.channels + c]);
-    const float st[3] = {s2, s1, s0};
-    for (int k = 0; t < 4; ++t, ++k) x[t] = st[k];
-    const float acc = w.w * x[0] + w.z * x[1] + w.y * x[2] + w.x * x[3];
-    p.y[(size_t)(q0 + j) * p.channels + c] = __float2bfloat16_rn(acc / (1.0f + __expf(-acc)));
-  }
+  float x[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    x[k] = k < on_tree ? bf2f(p.x[(size_t)(q0 + src[k]) * p.channels + c]) : bf2f(cs[2 - (k - on_tree)]);
+  const float acc = w.w * x[0] + w.z * x[1] + w.y * x[2] + w.x * x[3];
+  p.y[(size_t)row * p.channels + c] = __float2bfloat16_rn(acc / (1.0f + __expf(-acc)));
 }
 
 }  // namespace
 
-size_t gdn_smem_bytes(int max_nodes) { return GdnSmem::bytes(max_nodes); }
+size_t gdn_smem_bytes(int max_nodes) { return gdn_tree_smem(max_nodes); }
 
 cudaError_t launch_gdn_tree(const GdnParams& p, const BatchDesc& bd, cudaStream_t st) {
-  const size_t smem = GdnSmem::bytes(bd.max_nodes);
+  const size_t smem = gdn_tree_smem(bd.max_nodes);
   cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   gdn_tree_kernel<<<dim3(p.hv * (kD / kRows), bd.batch), kGdnThreads, smem, st>>>(p, bd);
@@ -337,7 +365,7 @@ cudaError_t launch_gdn_commit(const GdnCommitParams& p, const BatchDesc& bd, cud
 }
 
 cudaError_t launch_conv_tree(const ConvTreeParams& p, const BatchDesc& bd, cudaStream_t st) {
-  conv_tree_kernel<<<dim3((p.channels + 255) / 256, bd.batch), 256, 0, st>>>(p, bd);
+  conv_tree_kernel<<<dim3((p.channels + 255) / 256, bd.total_nodes), 256, 0, st>>>(p, bd);
   return cudaGetLastError();
 }
 
