@@ -31,12 +31,12 @@ namespace sdv {
 namespace {
 
 constexpr int kD = kGdnDim;        // d_k = d_v
-constexpr int kRows = 16;          // state rows per CTA
+constexpr int kCommitRows = 32;    // state rows per commit CTA
 constexpr int kLd = kD + 4;        // padded row (state, keys, queries): 8 consecutive rows read as float4 hit
                                    // 8 distinct 16-byte bank groups
 constexpr int kGdnThreads = 256;
 
-size_t gdn_tree_smem(int n) {
+size_t gdn_tree_smem(int n, int kRows) {
   return sizeof(float) * ((size_t)kRows * kLd + 2 * (size_t)n * kLd + (size_t)(4 * n + 1) * kRows +
                           2 * (size_t)n * (n + 1) + 4 * (size_t)n) +
          (size_t)n * kMaxNodes + sizeof(int) * 2 * (size_t)n;
@@ -60,6 +60,9 @@ __device__ __forceinline__ float dot128(const float* a, const float* b) {
   return (s0 + s1) + (s2 + s3);
 }
 
+// ROWS state rows per CTA: 16 when the batch is small (more CTAs), 64 when it is large (the fixed chain of
+// phases is paid once per 64 rows).
+template <int kRows>
 __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p, const BatchDesc bd) {
   extern __shared__ __align__(16) float smem[];
   const int b = blockIdx.y;
@@ -152,12 +155,10 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
     G[j] = lg;
     eg[j] = __expf(lg);
   }
-  {
-    const int r = tid & (kRows - 1);
-    for (int j = tid / kRows; j < n; j += kGdnThreads / kRows) {
-      W[j * kRows + r] = dot128(s0 + r * kLd, kh + j * kLd);
-      Z[j * kRows + r] = dot128(s0 + r * kLd, qh + j * kLd);
-    }
+  for (int i = tid; i < n * kRows; i += kGdnThreads) {
+    const int j = i / kRows, r = i % kRows;
+    W[i] = dot128(s0 + r * kLd, kh + j * kLd);
+    Z[i] = dot128(s0 + r * kLd, qh + j * kLd);
   }
   __syncthreads();
   // ---- pair coefficients along each node's path (row j, column = ancestor index; column n = padding 0)
@@ -175,24 +176,25 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
     }
   }
   __syncthreads();
-  // ---- u in node order (a node's ancestors come first): lane = row, four ancestors per round
-  if (warp == 0 && lane < kRows) {
+  // ---- u in node order (a node's ancestors come first): thread = row, four ancestors per round
+  if (tid < kRows) {
+    const int r = tid;
     for (int j = 0; j < n; ++j) {
-      float acc = beta[j] * (vv[j * kRows + lane] - eg[j] * W[j * kRows + lane]);
+      float acc = beta[j] * (vv[j * kRows + r] - eg[j] * W[j * kRows + r]);
       const uint8_t* al = alist + j * kMaxNodes;
       const float* aj = A + j * (n + 1);
       const int d = depth[j];
       for (int e = 0; e < d; e += 4) {
         const int m0 = al[e], m1 = al[e + 1], m2 = al[e + 2], m3 = al[e + 3];
         const float a0 = aj[m0], a1 = aj[m1], a2 = aj[m2], a3 = aj[m3];
-        const float u0 = U[m0 * kRows + lane], u1 = U[m1 * kRows + lane];
-        const float u2 = U[m2 * kRows + lane], u3 = U[m3 * kRows + lane];
+        const float u0 = U[m0 * kRows + r], u1 = U[m1 * kRows + r];
+        const float u2 = U[m2 * kRows + r], u3 = U[m3 * kRows + r];
         acc = fmaf(-a0, u0, acc);
         acc = fmaf(-a1, u1, acc);
         acc = fmaf(-a2, u2, acc);
         acc = fmaf(-a3, u3, acc);
       }
-      U[j * kRows + lane] = acc;
+      U[j * kRows + r] = acc;
     }
   }
   __syncthreads();
@@ -225,12 +227,12 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
 // S <- gamma_last S + sum over the accepted path of (gamma_last / gamma_m) u_m k_m^T,
 // 32 rows of one head per CTA, in place.
 __global__ void __launch_bounds__(kGdnThreads) gdn_commit_kernel(const GdnCommitParams p, const BatchDesc bd) {
-  __shared__ float ks[kMaxNodes][kD];      // normalised keys of the path (32 KB)
-  __shared__ float us[kMaxNodes][kRows];   // this block's u rows of the path
+  __shared__ __align__(16) float ks[kMaxNodes][kD];   // normalised keys of the path (32 KB)
+  __shared__ float us[kMaxNodes][kCommitRows];   // this block's u rows of the path
   __shared__ float wt[kMaxNodes];          // e^{G_last - G_m}
   __shared__ int bad;
   const int layer = blockIdx.z, b = blockIdx.y;
-  const int rb = blockIdx.x % (kD / kRows), h = blockIdx.x / (kD / kRows);
+  const int rb = blockIdx.x % (kD / kCommitRows), h = blockIdx.x / (kD / kCommitRows);
   const int hk = h / (p.hv / p.hk);
   const int q0 = bd.q_indptr[b];
   const int n = bd.q_indptr[b + 1] - q0;
@@ -256,9 +258,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_commit_kernel(const GdnCommit
     const int m = p.path[(size_t)b * p.max_path + i / kD];
     ks[i / kD][i % kD] = ck[((size_t)(q0 + m) * p.hk + hk) * kD + i % kD];
   }
-  for (int i = tid; i < a * kRows; i += kGdnThreads) {
-    const int m = p.path[(size_t)b * p.max_path + i / kRows];
-    us[i / kRows][i % kRows] = cu[((size_t)(q0 + m) * p.hv + h) * kD + rb * kRows + i % kRows];
+  for (int i = tid; i < a * kCommitRows; i += kGdnThreads) {
+    const int m = p.path[(size_t)b * p.max_path + i / kCommitRows];
+    us[i / kCommitRows][i % kCommitRows] = cu[((size_t)(q0 + m) * p.hv + h) * kD + rb * kCommitRows + i % kCommitRows];
   }
   for (int i = tid; i < a; i += kGdnThreads) {
     const int m = p.path[(size_t)b * p.max_path + i];
@@ -266,11 +268,20 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_commit_kernel(const GdnCommit
   }
   __syncthreads();
   const float gamma = __expf(g_last);
-  float* st = p.state[layer] + (((size_t)b * p.hv + h) * kD + rb * kRows) * kD;
-  for (int i = tid; i < kRows * kD; i += kGdnThreads) {
-    const int r = i / kD, c = i % kD;
-    float acc = gamma * st[i];
-    for (int m = 0; m < a; ++m) acc = fmaf(wt[m] * us[m][r], ks[m][c], acc);
+  // four consecutive columns per thread: 16-byte loads and stores of the state
+  float4* st = reinterpret_cast<float4*>(p.state[layer] + (((size_t)b * p.hv + h) * kD + rb * kCommitRows) * kD);
+  for (int i = tid; i < kCommitRows * kD / 4; i += kGdnThreads) {
+    const int r = (i * 4) / kD, c = (i * 4) % kD;
+    float4 acc = st[i];
+    acc.x *= gamma; acc.y *= gamma; acc.z *= gamma; acc.w *= gamma;
+    for (int m = 0; m < a; ++m) {
+      const float wu = wt[m] * us[m][r];
+      const float4 k4 = *reinterpret_cast<const float4*>(&ks[m][c]);
+      acc.x = fmaf(wu, k4.x, acc.x);
+      acc.y = fmaf(wu, k4.y, acc.y);
+      acc.z = fmaf(wu, k4.z, acc.z);
+      acc.w = fmaf(wu, k4.w, acc.w);
+    }
     st[i] = acc;
   }
 }
@@ -346,18 +357,29 @@ __global__ void __launch_bounds__(256) conv_tree_kernel(const ConvTreeParams p, 
 
 }  // namespace
 
-size_t gdn_smem_bytes(int max_nodes) { return gdn_tree_smem(max_nodes); }
+size_t gdn_smem_bytes(int max_nodes) { return gdn_tree_smem(max_nodes, 64); }
 
-cudaError_t launch_gdn_tree(const GdnParams& p, const BatchDesc& bd, cudaStream_t st) {
-  const size_t smem = gdn_tree_smem(bd.max_nodes);
-  cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int kRows>
+cudaError_t launch_gdn_rows(const GdnParams& p, const BatchDesc& bd, cudaStream_t st) {
+  const size_t smem = gdn_tree_smem(bd.max_nodes, kRows);
+  cudaError_t e =
+      cudaFuncSetAttribute(gdn_tree_kernel<kRows>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  gdn_tree_kernel<<<dim3(p.hv * (kD / kRows), bd.batch), kGdnThreads, smem, st>>>(p, bd);
+  gdn_tree_kernel<kRows><<<dim3(p.hv * (kD / kRows), bd.batch), kGdnThreads, smem, st>>>(p, bd);
   return cudaGetLastError();
 }
 
+cudaError_t launch_gdn_tree(const GdnParams& p, const BatchDesc& bd, cudaStream_t st) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 152;
+  // 16-row CTAs while they fit in about four per SM, else 64-row CTAs
+  const long long ctas16 = (long long)bd.batch * p.hv * (kD / 16);
+  return ctas16 <= 4LL * sms ? launch_gdn_rows<16>(p, bd, st) : launch_gdn_rows<64>(p, bd, st);
+}
+
 cudaError_t launch_gdn_commit(const GdnCommitParams& p, const BatchDesc& bd, cudaStream_t st) {
-  gdn_commit_kernel<<<dim3(p.hv * (kD / kRows), bd.batch, p.num_layers), kGdnThreads, 0, st>>>(p, bd);
+  gdn_commit_kernel<<<dim3(p.hv * (kD / kCommitRows), bd.batch, p.num_layers), kGdnThreads, 0, st>>>(p, bd);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.channels == 0) return e;
   conv_commit_kernel<<<dim3((p.channels + 255) / 256, bd.batch, p.num_layers), 256, 0, st>>>(p, bd);
