@@ -226,6 +226,43 @@ sd_status sd_accept(int batch, const int* q_indptr_h, int vocab, const float* lo
                     int* out_tokens, int* target_tokens, int max_path, void* workspace,
                     size_t ws_bytes, int* dev_status, void* stream);
 
+/* Bytes of workspace sd_sample_accept needs (0 on bad arguments). */
+size_t sd_sample_accept_workspace_size(int batch, const int* q_indptr_h, int vocab);
+
+/*
+ * sd_sample_accept — sampling-based verification (temperature T > 0) of every
+ * sequence's draft block, in place of sd_accept's greedy rule.
+ *
+ * The pages verify greedily and name sampling as future work ([S5] 补充测试 and
+ * 关键突破; [S3] runs at temperature 0) without an acceptance rule; this is
+ * standard speculative sampling with the multi-candidate rule for trees:
+ *   p_u = softmax(logits_u / T); the children of node u were drawn from the
+ *   draft distribution q_u = draft_probs[u]; they are tried in increasing node
+ *   order, child c with token x being accepted when r_accept[c] * q_u(x) <
+ *   p(x) (so with probability min(1, p(x) / q_u(x))); after a rejection p
+ *   becomes max(0, p - q_u), renormalised; the walk descends into an accepted
+ *   child; when every child of the current node is rejected, or it is a leaf,
+ *   the bonus token is the smallest v with sum_{w <= v} p(w) > r_sample[u] *
+ *   sum(p).  The emitted sequence is distributed as sampling from the target.
+ * Outputs follow sd_accept (accept length with the root counted, the path's
+ * node ids, the accepted drafts followed by the bonus token, -1 after A_b).
+ * Decisions are taken in fp32; a draft token outside [0, vocab) is never
+ * accepted.
+ *
+ *   vocab          V, 1..2048 * 1024
+ *   temperature    host float > 0 (finite)
+ *   logits         fp32 [sumN][V]
+ *   draft_probs    fp32 [sumN][V]   q at each node (rows of leaves are not read)
+ *   parents, draft_tokens   int32 [sumN]
+ *   r_accept, r_sample      fp32 [sumN], uniforms in [0, 1) (caller-drawn)
+ *   accept_len, path, out_tokens, max_path   as for sd_accept
+ */
+sd_status sd_sample_accept(int batch, const int* q_indptr_h, int vocab, float temperature, const float* logits,
+                           const float* draft_probs, const int* parents, const int* draft_tokens,
+                           const float* r_accept, const float* r_sample, int* accept_len, int* path,
+                           int* out_tokens, int max_path, void* workspace, size_t ws_bytes, int* dev_status,
+                           void* stream);
+
 /*
  * sd_kv_commit — append the accepted nodes' K/V to the cache, all layers in
  * one launch.  For every layer, sequence b and i < accept_len[b], node

@@ -312,6 +312,48 @@ sd_status sd_kv_commit_fp8(const sd_shape* shape, int num_layers, void* const* k
                    true);
 }
 
+size_t sd_sample_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {
+  BatchDesc bd;
+  if (fill_batch(batch, q_indptr_h, &bd) != SD_OK || vocab < 1) return 0;
+  const size_t chunks = ((size_t)vocab + kAcceptChunk - 1) / kAcceptChunk;
+  return align_up((size_t)bd.total_nodes * chunks * 8);
+}
+
+sd_status sd_sample_accept(int batch, const int* q_indptr_h, int vocab, float temperature, const float* logits,
+                           const float* draft_probs, const int* parents, const int* draft_tokens,
+                           const float* r_accept, const float* r_sample, int* accept_len, int* path,
+                           int* out_tokens, int max_path, void* workspace, size_t ws_bytes, int* dev_status,
+                           void* stream) {
+  BatchDesc bd;
+  sd_status st = fill_batch(batch, q_indptr_h, &bd);
+  if (st != SD_OK) return st;
+  if (vocab < 1 || max_path < 1 || !logits || !draft_probs || !parents || !draft_tokens || !r_accept ||
+      !r_sample || !accept_len || !path || !out_tokens)
+    return SD_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.0f / temperature))
+    return SD_ERR_INVALID_ARG;
+  if ((long long)vocab > (long long)kSampleMaxTiles * 1024) return SD_ERR_UNSUPPORTED;
+  const size_t need = sd_sample_accept_workspace_size(batch, q_indptr_h, vocab);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return SD_ERR_WORKSPACE;
+  SampleParams p;
+  p.logits = logits;
+  p.draft_probs = draft_probs;
+  p.parents = parents;
+  p.draft_tokens = draft_tokens;
+  p.r_accept = r_accept;
+  p.r_sample = r_sample;
+  p.accept_len = accept_len;
+  p.path = path;
+  p.out_tokens = out_tokens;
+  p.dev_status = dev_status;
+  p.partial = workspace;
+  p.vocab = vocab;
+  p.chunks = (vocab + kAcceptChunk - 1) / kAcceptChunk;
+  p.max_path = max_path;
+  p.inv_t = 1.0f / temperature;
+  return cuda_status(launch_sample_accept(p, bd, static_cast<cudaStream_t>(stream)));
+}
+
 size_t sd_gdn_tree_cache_size(const sd_gdn_shape* shape) {
   BatchDesc bd;
   if (check_gdn_shape(shape, &bd) != SD_OK) return 0;

@@ -40,6 +40,27 @@ struct AcceptParams {
 constexpr int kAcceptChunk = 4096;
 cudaError_t launch_accept(const AcceptParams& p, const BatchDesc& bd, cudaStream_t st);
 
+// Sampling-based verify: per-chunk softmax statistics, then one CTA per sequence walking its tree.
+constexpr int kSampleMaxTiles = 2048;   // vocabulary <= 2048 x 1024
+struct SampleParams {
+  const float* logits;        // [sumN][V] target logits
+  const float* draft_probs;   // [sumN][V] draft distribution at each node (its children were drawn from it)
+  const int* parents;
+  const int* draft_tokens;
+  const float* r_accept;      // [sumN] uniforms of the nodes' acceptance tests
+  const float* r_sample;      // [sumN] uniforms of a bonus drawn at the node
+  int* accept_len;
+  int* path;
+  int* out_tokens;
+  int* dev_status;            // nullable
+  void* partial;              // [sumN][chunks] (max, sum) pairs
+  int vocab;
+  int chunks;
+  int max_path;
+  float inv_t;                // 1 / temperature
+};
+cudaError_t launch_sample_accept(const SampleParams& p, const BatchDesc& bd, cudaStream_t st);
+
 // Commit of accepted K/V for all layers.
 struct CommitParams {
   void* k_cache[kMaxLayers];

@@ -80,6 +80,11 @@ def load() -> ctypes.CDLL:
     lib.sd_accept.restype = ctypes.c_int
     lib.sd_accept.argtypes = [ctypes.c_int, ip, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                               vp, sz, vp, vp]
+    lib.sd_sample_accept_workspace_size.restype = sz
+    lib.sd_sample_accept_workspace_size.argtypes = [ctypes.c_int, ip, ctypes.c_int]
+    lib.sd_sample_accept.restype = ctypes.c_int
+    lib.sd_sample_accept.argtypes = [ctypes.c_int, ip, ctypes.c_int, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, ctypes.c_int, vp, sz, vp, vp]
     lib.sd_kv_commit.restype = ctypes.c_int
     pp = ctypes.POINTER(ctypes.c_void_p)
     lib.sd_kv_commit.argtypes = [shp, ctypes.c_int, pp, pp, pp, pp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
@@ -204,6 +209,26 @@ def sd_accept(q_indptr, vocab: int, logits, parents, draft_tokens, accept_len, p
                             _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(target_tokens),
                             int(max_path), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
            "sd_accept")
+
+
+def sd_sample_accept_workspace_size(q_indptr, vocab: int) -> int:
+    ind = _indptr(q_indptr)
+    return int(load().sd_sample_accept_workspace_size(len(ind) - 1, ind, int(vocab)))
+
+
+def sd_sample_accept(q_indptr, vocab: int, temperature: float, logits, draft_probs, parents, draft_tokens, r_accept,
+                     r_sample, accept_len, path, out_tokens, max_path: int | None = None, workspace=None,
+                     dev_status=None, stream=None) -> None:
+    """Sampling-based verification at temperature T (speculative sampling, multi-candidate on trees)."""
+    ind = _indptr(q_indptr)
+    if max_path is None:
+        max_path = path.shape[-1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().sd_sample_accept(len(ind) - 1, ind, int(vocab), float(temperature), _ptr(logits), _ptr(draft_probs),
+                                   _ptr(parents), _ptr(draft_tokens), _ptr(r_accept), _ptr(r_sample),
+                                   _ptr(accept_len), _ptr(path), _ptr(out_tokens), int(max_path), _ptr(workspace),
+                                   ws_bytes, _ptr(dev_status), _stream(stream)),
+           "sd_sample_accept")
 
 
 def _ptr_array(ts) -> ctypes.Array:

@@ -29,7 +29,7 @@ def test_every_declared_symbol_is_exported(lib):
     for h in HEADERS:
         names |= set(re.findall(r"\b(sd_[a-z0-9_]+)\s*\(", open(h).read()))
     assert {"sd_verify_attn", "sd_accept", "sd_kv_commit", "sd_status_string", "sd_verify_attn_fp8",
-            "sd_kv_commit_fp8", "sd_gdn_tree", "sd_gdn_commit", "sd_gdn_conv_tree"} <= names
+            "sd_kv_commit_fp8", "sd_gdn_tree", "sd_gdn_commit", "sd_gdn_conv_tree", "sd_sample_accept"} <= names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -183,3 +183,18 @@ def test_gdn_host_checks(lib):
     ind2 = (ctypes.c_int * 2)(0, 23)
     assert lib.sd_gdn_conv_tree(1, ind2, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == native.SD_ERR_INVALID_ARG
     assert lib.sd_gdn_conv_tree(1, ind2, 64, None, FAKE, FAKE, FAKE, FAKE, None, None) == native.SD_ERR_INVALID_ARG
+
+
+def test_sample_accept_host_checks(lib):
+    ind = (ctypes.c_int * 2)(0, 23)
+    need = lib.sd_sample_accept_workspace_size(1, ind, 151936)
+    assert need >= 23 * 38 * 8
+    call = lambda vocab, t, ws=FAKE, nbytes=need, logits=FAKE: lib.sd_sample_accept(
+        1, ind, vocab, t, logits, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 17, ws, nbytes, None, None)
+    for bad_t in (0.0, -1.0, float("inf"), float("nan"), 1e-45):
+        assert call(151936, bad_t) == native.SD_ERR_INVALID_ARG, bad_t
+    assert call(0, 1.0) == native.SD_ERR_INVALID_ARG
+    assert call(2048 * 1024 + 1, 1.0) == native.SD_ERR_UNSUPPORTED
+    assert call(151936, 1.0, logits=None) == native.SD_ERR_INVALID_ARG
+    assert call(151936, 1.0, ws=None) == native.SD_ERR_WORKSPACE
+    assert call(151936, 1.0, nbytes=need - 1) == native.SD_ERR_WORKSPACE
