@@ -287,6 +287,54 @@ def time_gdn(dev, stream, w, reps: int) -> dict:
             "launches_per_step": 2 * GDN_LAYERS + 2}
 
 
+def time_sample_accept(dev, stream, w, reps: int, temperature: float = 1.0) -> dict:
+    """Sampling-based verify of the workload's draft blocks (in place of the greedy accept): the target logits
+    of the step, a draft distribution per node (softmax of the logits plus noise), drafts and uniforms drawn
+    once; timed from a CUDA graph."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    n, V = w.total_nodes, w.vocab
+    q = torch.softmax((w.logits + 0.5 * torch.randn((n, V), generator=g, device=dev)) / temperature, dim=-1)
+    parents = torch.as_tensor(w.parents, dtype=torch.int32, device=dev)
+    drafts = torch.as_tensor(w.draft_tokens, dtype=torch.int32, device=dev)
+    r_acc = torch.rand(n, generator=g, device=dev)
+    r_smp = torch.rand(n, generator=g, device=dev)
+    max_path = int(np.diff(w.q_indptr).max())
+    ws = torch.empty(native.sd_sample_accept_workspace_size(w.q_indptr, V), dtype=torch.uint8, device=dev)
+    lens = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    path = torch.empty((w.batch, max_path), dtype=torch.int32, device=dev)
+    toks = torch.empty((w.batch, max_path), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call(s):
+        native.sd_sample_accept(w.q_indptr, V, temperature, w.logits, q, parents, drafts, r_acc, r_smp, lens, path,
+                                toks, max_path, ws, status, stream=s)
+
+    gr = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(gr, stream=cap):
+            call(cap)
+    stream.wait_stream(cap)
+    for _ in range(3):
+        gr.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        gr.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the sampling verify")
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    # algorithmic bytes: the statistics pass reads the logits, the first-residual pass logits and draft rows
+    alg = n * V * 12
+    peak, _ = peaks()
+    return {"us": us, "temperature": temperature, "accepted_tokens": int(lens.sum().item()),
+            "alg_bytes": alg, "gbs": alg / (us * 1e-6) / 1e9, "frac": alg / (us * 1e-6) / 1e9 / peak, "launches": 3}
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -412,6 +460,7 @@ def run_ours(args, world, rank, local):
         line["ddtree_build"] = time_ddtree_build(dev, stream, w.batch, w.total_nodes // w.batch - 1)
     if not args.no_gdn:
         line["gdn_layers"] = time_gdn(dev, stream, w, reps=max(5, args.steps // 2))
+    line["sample_accept"] = time_sample_accept(dev, stream, w, reps=max(5, args.steps // 2))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.config, reps=1)
     return line

@@ -315,8 +315,8 @@ sd_status sd_kv_commit_fp8(const sd_shape* shape, int num_layers, void* const* k
 size_t sd_sample_accept_workspace_size(int batch, const int* q_indptr_h, int vocab) {
   BatchDesc bd;
   if (fill_batch(batch, q_indptr_h, &bd) != SD_OK || vocab < 1) return 0;
-  const size_t chunks = ((size_t)vocab + kAcceptChunk - 1) / kAcceptChunk;
-  return align_up((size_t)bd.total_nodes * chunks * 8);
+  const size_t chunks = ((size_t)vocab + kSampleTile - 1) / kSampleTile;
+  return align_up((size_t)bd.total_nodes * chunks * 8) + align_up((size_t)bd.total_nodes * chunks * 4);
 }
 
 sd_status sd_sample_accept(int batch, const int* q_indptr_h, int vocab, float temperature, const float* logits,
@@ -348,7 +348,8 @@ sd_status sd_sample_accept(int batch, const int* q_indptr_h, int vocab, float te
   p.dev_status = dev_status;
   p.partial = workspace;
   p.vocab = vocab;
-  p.chunks = (vocab + kAcceptChunk - 1) / kAcceptChunk;
+  p.chunks = (vocab + kSampleTile - 1) / kSampleTile;
+  p.resid = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up((size_t)bd.total_nodes * p.chunks * 8));
   p.max_path = max_path;
   p.inv_t = 1.0f / temperature;
   return cuda_status(launch_sample_accept(p, bd, static_cast<cudaStream_t>(stream)));

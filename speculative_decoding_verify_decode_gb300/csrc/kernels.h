@@ -41,6 +41,7 @@ constexpr int kAcceptChunk = 4096;
 cudaError_t launch_accept(const AcceptParams& p, const BatchDesc& bd, cudaStream_t st);
 
 // Sampling-based verify: per-chunk softmax statistics, then one CTA per sequence walking its tree.
+constexpr int kSampleTile = 1024;        // logits per tile of the statistics pass and of the inverse-CDF search
 constexpr int kSampleMaxTiles = 2048;   // vocabulary <= 2048 x 1024
 struct SampleParams {
   const float* logits;        // [sumN][V] target logits
@@ -53,7 +54,8 @@ struct SampleParams {
   int* path;
   int* out_tokens;
   int* dev_status;            // nullable
-  void* partial;              // [sumN][chunks] (max, sum) pairs
+  void* partial;              // [sumN][chunks] (max, sum) pairs per 1024-logit tile
+  float* resid;               // [sumN][chunks] per tile: sum of max(0, p - q) (the first residual)
   int vocab;
   int chunks;
   int max_path;

@@ -13,14 +13,18 @@
 //   every child is rejected (or u is a leaf) the bonus token is drawn from the
 //   current p by inverse CDF with u's uniform s_u.
 //
-// Kernel 1 scans 4096-entry chunks of every logits row (128-bit loads) for
-// the chunk's maximum and sum of exp((x - max) / T).  Kernel 2 runs one
-// 1024-thread CTA per sequence: it combines each row's chunk statistics, then
+// Kernel 1 scans 1024-entry tiles of every logits row (128-bit loads) for
+// the tile's maximum and sum of exp((x - max) / T).  Kernel 2 runs one
+// 1024-thread CTA per sequence: it combines each row's tile statistics, then
 // walks the tree with block-uniform decisions.  The current distribution is
 // kept as (node u, residual normalisers Z_1..Z_k): p_k(v) = max(0, p_{k-1}(v)
-// - q_u(v)) / Z_k with p_0 = p_u, recomputed element by element, so a
-// rejection costs one pass over the vocabulary (the next normaliser) and the
-// bonus one pass for tile sums plus one tile for the final scan.
+// - q_u(v)) / Z_k with p_0 = p_u, recomputed element by element.  A bonus
+// drawn with no residual step (the common case) needs no pass over the
+// vocabulary: the tile sums of p_u come from kernel 1, and one tile is
+// scanned.  Kernel 1b sums the first residual max(0, p_u - q_u) per tile for
+// every row, in parallel, so a first rejection at a node (its normaliser, and a
+// bonus drawn after it) needs no pass either; only a second rejection at the
+// same node costs passes over the vocabulary (16-byte loads).
 #include <climits>
 
 #include "common.cuh"
@@ -30,20 +34,21 @@ namespace sdv {
 namespace {
 
 constexpr int kSampleThreads = 1024;
-constexpr int kTile = 1024;              // elements per tile of the inverse-CDF search
+constexpr int kTile = kSampleTile;       // elements per tile (statistics and inverse-CDF search)
 constexpr int kMaxResidual = kMaxNodes;  // residual steps at one node (at most its children)
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct MaxSum {
   float m;
   float s;
 };
 
-// combine two (max, sum of exp((x - max) * inv_t)) pairs
-__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float inv_t) {
+// combine two (max, sum of exp((x - max) / T)) pairs; c = log2(e) / T, so exp(y / T) = 2^(y c)
+__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float c) {
   if (a.m == -INFINITY) return b;
   if (b.m == -INFINITY) return a;
   const float m = fmaxf(a.m, b.m);
-  return {m, a.s * expf((a.m - m) * inv_t) + b.s * expf((b.m - m) * inv_t)};
+  return {m, a.s * fast_exp2((a.m - m) * c) + b.s * fast_exp2((b.m - m) * c)};
 }
 
 template <bool kVec4>
@@ -51,18 +56,18 @@ __global__ void __launch_bounds__(256) lse_chunk_kernel(const SampleParams p) {
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const float* x = p.logits + (size_t)row * p.vocab;
-  const int begin = chunk * kAcceptChunk;
-  const int end = min(p.vocab, begin + kAcceptChunk);
-  const float inv_t = p.inv_t;
+  const int begin = chunk * kTile;
+  const int end = min(p.vocab, begin + kTile);
+  const float inv_t = p.inv_t * kLog2e;   // base-2 scale
   MaxSum acc = {-INFINITY, 0.f};
   bool nan = false;
   auto add = [&](float e) {
     nan |= e != e;
     if (e > acc.m) {
-      acc.s = acc.m == -INFINITY ? 1.f : acc.s * expf((acc.m - e) * inv_t) + 1.f;
+      acc.s = acc.m == -INFINITY ? 1.f : acc.s * fast_exp2((acc.m - e) * inv_t) + 1.f;
       acc.m = e;
     } else if (e != -INFINITY) {
-      acc.s += expf((e - acc.m) * inv_t);
+      acc.s += fast_exp2((e - acc.m) * inv_t);
     }
   };
   if (kVec4) {
@@ -88,6 +93,56 @@ __global__ void __launch_bounds__(256) lse_chunk_kernel(const SampleParams p) {
   }
 }
 
+// Per (row, tile): sum of max(0, p_u(v) - q_u(v)) over the tile's tokens — the tile sums of the first
+// residual at every node, from which the walk takes the first normaliser and, after one rejection, the
+// bonus tile sums without a pass of its own.
+template <bool kVec4>
+__global__ void __launch_bounds__(256) resid_tile_kernel(const SampleParams p) {
+  const int row = blockIdx.y, tile = blockIdx.x;
+  const float c = p.inv_t * kLog2e;
+  __shared__ float s_stat[2];
+  __shared__ float red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {   // the row's statistics from its tile partials
+    const MaxSum* part = reinterpret_cast<const MaxSum*>(p.partial) + (size_t)row * p.chunks;
+    MaxSum acc = {-INFINITY, 0.f};
+    for (int t = lane; t < p.chunks; t += 32) acc = combine(acc, part[t], c);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      MaxSum o = {__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.s, off)};
+      acc = combine(acc, o, c);
+    }
+    if (lane == 0) {
+      s_stat[0] = acc.m;
+      s_stat[1] = acc.s > 0.f ? 1.0f / acc.s : 0.f;
+    }
+  }
+  __syncthreads();
+  const float m = s_stat[0], inv_s = s_stat[1];
+  const float* lr = p.logits + (size_t)row * p.vocab;
+  const float* qr = p.draft_probs + (size_t)row * p.vocab;
+  const int v0 = tile * kSampleTile + threadIdx.x * 4;
+  float r = 0.f;
+  if (kVec4 && v0 + 4 <= p.vocab) {
+    const float4 l = *reinterpret_cast<const float4*>(lr + v0);
+    const float4 q = *reinterpret_cast<const float4*>(qr + v0);
+    r = fmaxf(fast_exp2((l.x - m) * c) * inv_s - q.x, 0.f) + fmaxf(fast_exp2((l.y - m) * c) * inv_s - q.y, 0.f) +
+        fmaxf(fast_exp2((l.z - m) * c) * inv_s - q.z, 0.f) + fmaxf(fast_exp2((l.w - m) * c) * inv_s - q.w, 0.f);
+  } else {
+    for (int i = 0; i < 4 && v0 + i < p.vocab; ++i)
+      r += fmaxf(fast_exp2((lr[v0 + i] - m) * c) * inv_s - qr[v0 + i], 0.f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  if (lane == 0) red[warp] = r;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    p.resid[(size_t)row * p.chunks + tile] = t;
+  }
+}
+
 // Sum of one value per thread over the block; every thread gets the total.
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -102,16 +157,18 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-__global__ void __launch_bounds__(kSampleThreads) sample_accept_kernel(const SampleParams p, const BatchDesc bd) {
+// kVec4: V % 4 == 0 and 16-byte aligned rows, so passes move four tokens per 16-byte load.
+template <bool kVec4>
+__global__ void __launch_bounds__(kSampleThreads, 1) sample_accept_kernel(const SampleParams p, const BatchDesc bd) {
   const int b = blockIdx.x;
   const int q0 = bd.q_indptr[b];
   const int n = bd.q_indptr[b + 1] - q0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int V = p.vocab;
-  const float inv_t = p.inv_t;
-  __shared__ float s_m[kMaxNodes], s_s[kMaxNodes];   // per row: max, sum of exp((x - max) / T)
+  const float inv_t = p.inv_t * kLog2e;   // base-2 scale: exp((x - m) / T) = 2^((x - m) * inv_t)
+  __shared__ float s_m[kMaxNodes], s_s[kMaxNodes];   // per row: max, 1 / sum of exp((x - max) / T) (0 if none)
   __shared__ int s_par[kMaxNodes], s_path[kMaxNodes + 1], s_tok[kMaxNodes + 1];
-  __shared__ float s_z[kMaxResidual];                // residual normalisers at the current node
+  __shared__ float s_z[kMaxResidual];                // reciprocals of the residual normalisers at the current node
   __shared__ float s_red[kSampleThreads / 32];
   __shared__ float s_tiles[kSampleMaxTiles];
   __shared__ int s_bad, s_pick;
@@ -130,7 +187,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_accept_kernel(const Sam
     }
     if (lane == 0) {
       s_m[row] = acc.m;
-      s_s[row] = acc.s;
+      s_s[row] = acc.s > 0.f ? 1.0f / acc.s : 0.f;
     }
   }
   if (tid < n) {
@@ -143,13 +200,40 @@ __global__ void __launch_bounds__(kSampleThreads) sample_accept_kernel(const Sam
   const bool bad = s_bad != 0;
   if (bad && tid == 0) report(p.dev_status, SD_DEV_BAD_PARENTS);
 
-  // p_k(v) at node u with k residual steps
-  auto prob = [&](int u, int k, int v) -> float {
-    const float l = p.logits[(size_t)(q0 + u) * V + v];
-    float x = s_s[u] > 0.f ? expf((l - s_m[u]) * inv_t) / s_s[u] : 0.f;
-    const float qv = p.draft_probs[(size_t)(q0 + u) * V + v];
-    for (int i = 0; i < k; ++i) x = fmaxf(x - qv, 0.f) / s_z[i];
+  // p_k(v) at node u with k residual steps, from the logit l and the draft probability qv of token v
+  auto prob_of = [&](int u, int k, float l, float qv) -> float {
+    float x = fast_exp2((l - s_m[u]) * inv_t) * s_s[u];
+    for (int i = 0; i < k; ++i) x = fmaxf(x - qv, 0.f) * s_z[i];
     return x;
+  };
+  auto prob = [&](int u, int k, int v) -> float {
+    return prob_of(u, k, p.logits[(size_t)(q0 + u) * V + v], p.draft_probs[(size_t)(q0 + u) * V + v]);
+  };
+  // sum over tokens [v0, v0 + 32) of p_k (tile-sum pass) or of max(0, p_k - q) (next normaliser)
+  auto sum32 = [&](int u, int k, int v0, bool resid) -> float {
+    float acc = 0.f;
+    const float* lr = p.logits + (size_t)(q0 + u) * V;
+    const float* qr = p.draft_probs + (size_t)(q0 + u) * V;
+    if (kVec4 && v0 + 32 <= V) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 l = *reinterpret_cast<const float4*>(lr + v0 + i);
+        const float4 q = *reinterpret_cast<const float4*>(qr + v0 + i);
+        const float e[4] = {l.x, l.y, l.z, l.w}, f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float x = prob_of(u, k, e[c], f[c]);
+          acc += resid ? fmaxf(x - f[c], 0.f) : x;
+        }
+      }
+    } else {
+      for (int i = 0; i < 32 && v0 + i < V; ++i) {
+        const float f = qr[v0 + i];
+        const float x = prob_of(u, k, lr[v0 + i], f);
+        acc += resid ? fmaxf(x - f, 0.f) : x;
+      }
+    }
+    return acc;
   };
 
   int u = 0, k = 0, a = 1;
@@ -167,14 +251,18 @@ __global__ void __launch_bounds__(kSampleThreads) sample_accept_kernel(const Sam
         accepted = c;
         break;
       }
-      // rejected: the next residual normaliser, one pass over the vocabulary
+      // rejected: the next residual normaliser — the first from the residual tile sums, later ones by a
+      // pass over the vocabulary (32 tokens per thread and round)
       float part = 0.f;
-      for (int v = tid; v < V; v += kSampleThreads)
-        part += fmaxf(prob(u, k, v) - p.draft_probs[(size_t)(q0 + u) * V + v], 0.f);
+      if (k == 0) {
+        for (int t = tid; t < p.chunks; t += kSampleThreads) part += p.resid[(size_t)(q0 + u) * p.chunks + t];
+      } else {
+        for (int v0 = tid * 32; v0 < V; v0 += kSampleThreads * 32) part += sum32(u, k, v0, true);
+      }
       const float z = block_sum(part, s_red);
       if (z > 0.f && k < kMaxResidual) {
         __syncthreads();
-        if (tid == 0) s_z[k] = z;
+        if (tid == 0) s_z[k] = 1.0f / z;
         __syncthreads();
         ++k;
       }
@@ -189,18 +277,25 @@ __global__ void __launch_bounds__(kSampleThreads) sample_accept_kernel(const Sam
       k = 0;
       continue;
     }
-    // bonus from the current distribution: tile sums (a warp per tile, lane = 32 consecutive tokens),
-    // then the tile and the token where the cumulative sum first exceeds s * total
+    // bonus from the current distribution: tile sums — from the statistics pass when no residual step
+    // was taken, else one pass (a warp per tile, lane = 32 consecutive tokens) — then the tile and the
+    // token where the cumulative sum first exceeds s * total
     const int tiles = (V + kTile - 1) / kTile;
-    for (int t = warp; t < tiles; t += kSampleThreads / 32) {
-      float ls = 0.f;
-      for (int i = 0; i < 32; ++i) {
-        const int v = t * kTile + lane * 32 + i;
-        if (v < V) ls += prob(u, k, v);
+    if (k == 0) {
+      const MaxSum* part = reinterpret_cast<const MaxSum*>(p.partial) + (size_t)(q0 + u) * p.chunks;
+      for (int t = tid; t < tiles; t += kSampleThreads) {
+        const MaxSum ms = part[t];
+        s_tiles[t] = ms.m == -INFINITY ? 0.f : ms.s * fast_exp2((ms.m - s_m[u]) * inv_t) * s_s[u];
       }
+    } else if (k == 1) {
+      for (int t = tid; t < tiles; t += kSampleThreads) s_tiles[t] = p.resid[(size_t)(q0 + u) * p.chunks + t] * s_z[0];
+    } else {
+      for (int t = warp; t < tiles; t += kSampleThreads / 32) {
+        float ls = sum32(u, k, t * kTile + lane * 32, false);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-      if (lane == 0) s_tiles[t] = ls;
+        for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+        if (lane == 0) s_tiles[t] = ls;
+      }
     }
     __syncthreads();
     if (tid == 0) {
@@ -286,7 +381,13 @@ cudaError_t launch_sample_accept(const SampleParams& p, const BatchDesc& bd, cud
   else lse_chunk_kernel<false><<<grid, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sample_accept_kernel<<<bd.batch, kSampleThreads, 0, st>>>(p, bd);
+  const bool vec = p.vocab % 4 == 0 && aligned && (reinterpret_cast<uintptr_t>(p.draft_probs) & 15) == 0;
+  if (vec) resid_tile_kernel<true><<<grid, 256, 0, st>>>(p);
+  else resid_tile_kernel<false><<<grid, 256, 0, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (vec) sample_accept_kernel<true><<<bd.batch, kSampleThreads, 0, st>>>(p, bd);
+  else sample_accept_kernel<false><<<bd.batch, kSampleThreads, 0, st>>>(p, bd);
   return cudaGetLastError();
 }
 
