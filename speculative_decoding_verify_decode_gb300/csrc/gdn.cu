@@ -39,26 +39,28 @@ constexpr int kGdnThreads = 256;
 size_t gdn_tree_smem(int n, int kRows) {
   return sizeof(float) * ((size_t)kRows * kLd + 2 * (size_t)n * kLd + (size_t)(4 * n + 1) * kRows +
                           2 * (size_t)n * (n + 1) + 4 * (size_t)n) +
-         (size_t)n * kMaxNodes + sizeof(int) * 2 * (size_t)n;
+         (size_t)n * kMaxNodes + sizeof(int) * (3 * (size_t)n + 1);
 }
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// 128-element dot product of two padded shared-memory rows (float4 loads, four partial sums).
-__device__ __forceinline__ float dot128(const float* a, const float* b) {
+// Two 128-element dot products sharing their first row: (a . b, a . c), each row read once (float4 loads).
+__device__ __forceinline__ float2 dot128x2(const float* a, const float* b, const float* c) {
   const float4* a4 = reinterpret_cast<const float4*>(a);
   const float4* b4 = reinterpret_cast<const float4*>(b);
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  const float4* c4 = reinterpret_cast<const float4*>(c);
+  float s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
 #pragma unroll 8
   for (int t = 0; t < kD / 4; ++t) {
-    const float4 x = a4[t], y = b4[t];
-    s0 = fmaf(x.x, y.x, s0);
-    s1 = fmaf(x.y, y.y, s1);
-    s2 = fmaf(x.z, y.z, s2);
-    s3 = fmaf(x.w, y.w, s3);
+    const float4 x = a4[t], y = b4[t], z = c4[t];
+    s0 = fmaf(x.x, y.x, fmaf(x.y, y.y, s0));
+    s1 = fmaf(x.z, y.z, fmaf(x.w, y.w, s1));
+    t0 = fmaf(x.x, z.x, fmaf(x.y, z.y, t0));
+    t1 = fmaf(x.z, z.z, fmaf(x.w, z.w, t1));
   }
-  return (s0 + s1) + (s2 + s3);
+  return make_float2(s0 + s1, t0 + t1);
 }
+
 
 // ROWS state rows per CTA: 16 when the batch is small (more CTAs), 64 when it is large (the fixed chain of
 // phases is paid once per 64 rows).
@@ -88,7 +90,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
   float* eg = gg + n;                            // [n] e^{G_j}
   int* par = reinterpret_cast<int*>(eg + n);     // [n]
   int* depth = par + n;                          // [n] proper ancestors of j
-  uint8_t* alist = reinterpret_cast<uint8_t*>(depth + n);   // [n][64] proper ancestors, padded with n
+  int* poff = depth + n;                         // [n + 1] offsets of each node's (node, path member) pairs
+  uint8_t* alist = reinterpret_cast<uint8_t*>(poff + n + 1);   // [n][64] proper ancestors, padded with n
 
   // ---- every global load of the CTA, before any barrier
   {
@@ -155,21 +158,46 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_tree_kernel(const GdnParams p
     G[j] = lg;
     eg[j] = __expf(lg);
   }
+  __syncthreads();
+  if (tid < 32) {   // offsets of the compacted (node, path member) pairs: node j owns depth[j] + 1 of them
+    int run = 0;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + tid;
+      const int cnt = j < n ? depth[j] + 1 : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += o;
+      }
+      if (j < n) poff[j] = run + incl - cnt;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (tid == 0) poff[n] = run;
+  }
+  // S_0 k_j and S_0 q_j: one thread per (node, row), the row read once for both products
   for (int i = tid; i < n * kRows; i += kGdnThreads) {
     const int j = i / kRows, r = i % kRows;
-    W[i] = dot128(s0 + r * kLd, kh + j * kLd);
-    Z[i] = dot128(s0 + r * kLd, qh + j * kLd);
+    const float2 wz = dot128x2(s0 + r * kLd, kh + j * kLd, qh + j * kLd);
+    W[i] = wz.x;
+    Z[i] = wz.y;
   }
   __syncthreads();
-  // ---- pair coefficients along each node's path (row j, column = ancestor index; column n = padding 0)
-  for (int i = tid; i < n * kMaxNodes; i += kGdnThreads) {
-    const int j = i / kMaxNodes, e = i % kMaxNodes;
+  // ---- pair coefficients along each node's path (row j, column = ancestor index; column n = padding 0),
+  // one thread per (node, path member) pair
+  for (int i = tid; i < poff[n]; i += kGdnThreads) {
+    int lo = 0, hi = n - 1;   // node j with poff[j] <= i < poff[j + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (poff[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    const int j = lo, e = i - poff[j];
     const int d = depth[j];
-    if (e > d) continue;
     const int m = e < d ? alist[j * kMaxNodes + e] : j;   // the ancestors, then j itself
     const float ratio = __expf(G[j] - G[m]);
-    if (m != j) A[j * (n + 1) + m] = beta[j] * ratio * dot128(kh + m * kLd, kh + j * kLd);
-    C[j * (n + 1) + m] = ratio * dot128(kh + m * kLd, qh + j * kLd);
+    const float2 kq = dot128x2(kh + m * kLd, kh + j * kLd, qh + j * kLd);
+    if (m != j) A[j * (n + 1) + m] = beta[j] * ratio * kq.x;
+    C[j * (n + 1) + m] = ratio * kq.y;
     if (e == 0) {
       A[j * (n + 1) + n] = 0.f;
       C[j * (n + 1) + n] = 0.f;
