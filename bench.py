@@ -383,7 +383,8 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(attn_graph, stream=cap):
             for layer in range(w.layers):
                 step.attention(layer, w.q[layer], w.k_cache[layer], w.v_cache[layer], w.k_new[layer],
-                               w.v_new[layer], d["page_table"], d["ctx_lens"], d["parents"], stream=cap)
+                               w.v_new[layer], d["page_table"], d["ctx_lens"], d["parents"], stream=cap,
+                               ctx_stable=layer > 0)
     stream.wait_stream(cap)
     for _ in range(3):
         attn_graph.replay()

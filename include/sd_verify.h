@@ -99,6 +99,15 @@ typedef struct sd_shape {
                                 positions > L + depth(j) - W, its W most recent ones (own key included);
                                 0 = the whole context.  Source: «如何在单张 RTX 3090 上让 Qwen3.5-27B token
                                 生成速度提升 6 倍», 补充测试 (attention over the most recent 2,048 positions). */
+  int ctx_stable;            /* sd_verify_attn / sd_verify_attn_fp8 only; other calls ignore it.  Nonzero: the
+                                caller guarantees that the kernel issued just before this call on its stream
+                                writes none of ctx_lens, page_table and the pool pages holding positions
+                                [0, L_b) — true for every layer of a step after the first, whose predecessor
+                                is the previous layer's attention.  The context CTAs then read those and start
+                                their cache loads before they wait for that kernel to finish (programmatic
+                                dependent launch); q, k_new, v_new, parents, the outputs and the workspace are
+                                still touched only after the wait.  0: everything waits (always safe, e.g.
+                                for the first layer after the previous step's commit). */
 } sd_shape;
 
 /* Human-readable name of a status code (static string). */

@@ -167,6 +167,7 @@ sd_status verify_attn(const sd_shape* shape, const void* q, const void* k_cache,
   p.chunk = pl.chunk;
   p.num_splits = pl.nsplit;
   p.window = shape->window;
+  p.ctx_stable = shape->ctx_stable != 0;
   if (need > 0) {
     const size_t rows = (size_t)pl.nsplit * bd.total_nodes * kHq;
     p.o_part = static_cast<__nv_bfloat16*>(workspace);

@@ -31,6 +31,10 @@ constexpr int kMergeGroups = kMergeThreads / 64;
 constexpr int kBatch = 12;
 
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p, const BatchDesc bd) {
+  // The next kernel in the stream (the next layer's split kernel) may be
+  // scheduled at once; it waits for this grid before it reads what this grid
+  // writes, and may load context tiles meanwhile.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int pair = blockIdx.x;
   const int r = pair / kHq, head = pair % kHq;
   int lo = 0, hi = bd.batch - 1;   // sequence of node row r
@@ -41,9 +45,12 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   int L = p.ctx_lens[lo];
   L = L < 0 ? 0 : min(L, p.max_pages * kPage);
   const int ns = active_splits(L, p.window, kTileTokens, p.chunk);
-  if (ns == 1) return;  // written directly by the split kernel
-  // the partials are written by the split kernel launched just before
+  // The partials are written by the split kernel launched just before.  Every
+  // block waits for it, even one with nothing to merge, so that this grid
+  // finishes only after the split kernel: a dependent that waits for this grid
+  // then also sees the outputs the split kernel wrote directly.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (ns == 1) return;  // written directly by the split kernel
   const size_t stride = (size_t)bd.total_nodes * kHq;   // rows between splits
   const size_t row0 = (size_t)r * kHq + head;
   __shared__ float4 s_acc[kMergeGroups][64];
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
 
 // Launched as a programmatic dependent of the split kernel: its blocks may be
 // scheduled while the split kernel runs and wait (griddepcontrol.wait) for
-// that kernel's completion before they read the partials.
+// that kernel's completion before they read the partials.  It lets its own
+// dependents be scheduled at once (see the kernel).
 cudaError_t launch_attn_merge(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(bd.total_nodes * kHq);

@@ -164,12 +164,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false (and the CTA's abort flag set) if the phase never completes.
+// Status bits from a thread that may not have waited for the previous kernel
+// yet (context loads issued before the wait): wait first, so that the bit
+// cannot be lost to a predecessor that resets the status word.  A no-op wait
+// once the predecessor has finished.
+__device__ __forceinline__ void report_dep(int* status, int bits) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  report(status, bits);
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Small* sm, int* status) {
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
       sm->abort = 1;
-      report(status, SD_DEV_TIMEOUT);
+      report_dep(status, SD_DEV_TIMEOUT);
       return false;
     }
   }
@@ -182,7 +190,7 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, Small* 
   while (!mbar_test(bar, parity)) {
     if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
       sm->abort = 1;
-      report(status, SD_DEV_TIMEOUT);
+      report_dep(status, SD_DEV_TIMEOUT);
       return false;
     }
   }
@@ -393,14 +401,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_nodes = bd.q_indptr[b + 1] - q0;
   const int rows = hpc * n_nodes;
   if (c * hpc >= kGroup) return;
-  // Launched as a programmatic dependent: wait for the previous kernel in the
-  // stream before touching global memory, then let the merge kernel's blocks
-  // be scheduled (they wait for this grid to finish before reading).
+  // Launched as a programmatic dependent of the previous kernel in the stream.
+  // By default every thread waits for that kernel before touching global
+  // memory.  With ctx_stable (the caller guarantees that kernel writes neither
+  // the context lengths, the page table nor the context pages) a context CTA
+  // reads those and issues its first tile's loads first: its producers wait
+  // once that tile is on its way, its compute warps before they read Q or the
+  // parents, so the outputs and the workspace are written only after the wait.
+  // The draft CTA always waits here: it reads Q and the draft block at once.
+  // Then the merge kernel's blocks may be scheduled (they wait for this grid to
+  // finish before reading).
+  const bool early = p.ctx_stable != 0 && s != 0;
   // the producers fetch their TMA descriptor while the rest of the prologue runs
   if (((!KV8 && (warp == kWarpK || warp == kWarpV)) || (KV8 && warp == kWarpLoad)) && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpV ? &tm_v : &tm_k))
                  : "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Split 0 attends to the draft block alone; split s >= 1 to context tokens
   // [(s - 1) * chunk, s * chunk).  The producers fetch their first tile's page
@@ -430,7 +446,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
   const int head0 = g * kGroup + c * hpc;
   if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
-    if (threadIdx.x == 0) report(p.dev_status, SD_DEV_TIMEOUT);
+    if (threadIdx.x == 0) report_dep(p.dev_status, SD_DEV_TIMEOUT);
     return;
   }
 
@@ -456,7 +472,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
   }
   // one load each; the walks below are in shared memory (every CTA needs the depths with a window)
-  if ((has_draft || W > 0) && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];
+  // (an early context CTA's compute warps load them after their wait)
+  if ((has_draft || (W > 0 && !early)) && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];
   __syncthreads();  // mbarriers and per-column arrays ready
   const uint32_t bars = smem_u32(&sm->bar[0]);
   auto bar = [&](int i) { return bars + 8u * i; };
@@ -535,7 +552,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
         page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
       if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
-        if (report_bad) report(p.dev_status, SD_DEV_BAD_PAGE);
+        if (report_bad) report_dep(p.dev_status, SD_DEV_BAD_PAGE);
         page = -1;
       }
       return page;
@@ -579,13 +596,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
           if (todo != 0) {
             if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
-              if (lane == 0) { sm->abort = 1; report(p.dev_status, SD_DEV_TIMEOUT); }
+              if (lane == 0) { sm->abort = 1; report_dep(p.dev_status, SD_DEV_TIMEOUT); }
               ok = false;
               break;
             }
             __nanosleep(20);
           }
         }
+        // early context loads: the next slots free up only as the compute warps (which wait) progress
+        if (early && i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
       }
       // no copy may still be landing when the CTA ends (after an abort): wait, bounded, for the last of each slot
       if (lane == 0) {
@@ -634,6 +653,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const int page = tile_pages(i, valid, false);
         const bool whole = valid == kT && __ballot_sync(0xffffffffu, lane < 8 && page >= 0) == 0xffu;
         for (int h = 0; h < 2; ++h, ++uses) {
+          // early context loads: the f16 buffer's second use waits for the compute warps (which wait)
+          if (early && uses == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
           const uint32_t slot_full = bar(is_k ? K8_FULL0 + h : V8_FULL0 + h);
           const uint32_t buf_empty = bar(is_k ? K_EMPTY : V_EMPTY0);
           if (lane == 0)
@@ -712,7 +733,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
         page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
       if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
-        report(p.dev_status, SD_DEV_BAD_PAGE);
+        report_dep(p.dev_status, SD_DEV_BAD_PAGE);
         page = -1;
       }
       // a page goes by TMA when it is in range and all 16 of its tokens are valid
@@ -743,6 +764,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (((part_mask & tma_mask) >> lane) & 1u)
           tma_load_page(smem_u32(dst + lane * kPageB), map, (page * kHkv + g) * 2, full);
       }
+      // early context loads: the next tile's buffers free up only as the compute warps (which wait) progress
+      if (early && i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
       if (!ok) break;
       if (__shfl_sync(0xffffffffu, sm->abort, 0)) break;
     }
@@ -752,6 +775,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // (and split 0's draft block, tile 0) and allocate tensor memory.
   {
     const int ct = tid - 32;
+    if (early) {
+      // tensor memory first (no global memory), then the wait for the previous kernel
+      if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      // the window depths need the parents (ordered before their use by the staging barrier)
+      if (W > 0)
+        for (int j = ct; j < n_nodes; j += 5 * 32) sm->par[j] = p.parents[q0 + j];
+    }
     if (!has_draft) stage_operands(ct, 5 * 32, false);
     if (W > 0) {
       // oldest visible context position of each query column: L + depth(node) - W + 1
@@ -769,7 +803,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         sm->lo_col[q] = L + d - W + 1;
       }
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma && !early) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }

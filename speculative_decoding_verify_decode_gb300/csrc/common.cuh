@@ -52,6 +52,7 @@ struct AttnParams {
   int chunk;             // context tokens per split (multiple of the kernel's tile)
   int num_splits;
   int window;            // sliding window (0: the whole context)
+  int ctx_stable;        // context CTAs may read the table and cache pages before the wait on the previous kernel
   // e4m3 caches (the quantised path): code c of K / V stands for decode(c) * k_scale / v_scale
   const uint8_t* k_cache8;
   const uint8_t* v_cache8;

@@ -36,7 +36,7 @@ class SdShape(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("max_pages_per_seq", ctypes.c_int), ("num_pool_pages", ctypes.c_int),
                 ("num_splits", ctypes.c_int),
-                ("window", ctypes.c_int)]
+                ("window", ctypes.c_int), ("ctx_stable", ctypes.c_int)]
 
 
 class SdGdnShape(ctypes.Structure):
@@ -145,11 +145,17 @@ class Shape:
     """An sd_shape with its host q_indptr kept alive."""
 
     def __init__(self, q_indptr, max_pages_per_seq: int, num_pool_pages: int, num_splits: int = 0,
-                 window: int = 0):
+                 window: int = 0, ctx_stable: bool = False):
         self.indptr = _indptr(q_indptr)
         self.c = SdShape(len(self.indptr) - 1, ctypes.cast(self.indptr, ctypes.POINTER(ctypes.c_int)),
                          24, 4, 256, 16, int(max_pages_per_seq), int(num_pool_pages), int(num_splits),
-                         int(window))
+                         int(window), int(bool(ctx_stable)))
+
+    def with_ctx_stable(self, ctx_stable: bool = True) -> "Shape":
+        """The same shape with the context-stable launch flag set (see sd_shape.ctx_stable)."""
+        c = self.c
+        return Shape(list(self.indptr), c.max_pages_per_seq, c.num_pool_pages, c.num_splits, c.window,
+                     ctx_stable)
 
     @property
     def ref(self):

@@ -29,6 +29,8 @@ class VerifyStep:
         self.vocab = int(vocab)
         self.device = torch.device(device)
         self.shape = native.Shape(self.q_indptr, max_pages_per_seq, num_pool_pages, num_splits, window)
+        # layers after the first follow the previous layer's attention, which writes no context state
+        self.shape_next = self.shape.with_ctx_stable(True)
         self.fp8 = k_scales is not None
         if self.fp8 and (v_scales is None or len(k_scales) != self.num_layers or len(v_scales) != self.num_layers):
             raise ValueError("e4m3 caches need one K and one V scale per layer")
@@ -51,14 +53,18 @@ class VerifyStep:
         self.new_ctx_lens = torch.empty(self.batch, dtype=torch.int32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def attention(self, layer, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, stream=None):
+    def attention(self, layer, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents, stream=None,
+                  ctx_stable: bool = False):
+        """One layer's attention.  ``ctx_stable``: the previous kernel on the stream writes no context state
+        (sd_shape.ctx_stable), so the context loads may start before it finishes."""
         lse = None if self.lse is None else self.lse[layer]
+        shape = self.shape_next if ctx_stable else self.shape
         if self.fp8:
-            native.sd_verify_attn_fp8(self.shape, q, k_cache, v_cache, self.k_scales[layer], self.v_scales[layer],
+            native.sd_verify_attn_fp8(shape, q, k_cache, v_cache, self.k_scales[layer], self.v_scales[layer],
                                       k_new, v_new, page_table, ctx_lens, parents, self.out[layer], lse,
                                       self.attn_ws, self.dev_status, stream)
         else:
-            native.sd_verify_attn(self.shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents,
+            native.sd_verify_attn(shape, q, k_cache, v_cache, k_new, v_new, page_table, ctx_lens, parents,
                                   self.out[layer], lse, self.attn_ws, self.dev_status, stream)
 
     def accept(self, logits, parents, draft_tokens, stream=None):
@@ -81,7 +87,7 @@ class VerifyStep:
         """q/k_caches/v_caches/k_news/v_news are per-layer lists of device tensors."""
         for layer in range(self.num_layers):
             self.attention(layer, q[layer], k_caches[layer], v_caches[layer], k_news[layer], v_news[layer],
-                           page_table, ctx_lens, parents, stream)
+                           page_table, ctx_lens, parents, stream, ctx_stable=layer > 0)
         self.accept(logits, parents, draft_tokens, stream)
         if commit:
             self.commit(k_caches, v_caches, k_news, v_news, page_table, ctx_lens, stream)

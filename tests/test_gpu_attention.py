@@ -94,3 +94,85 @@ def test_full_size_sampled(name):
     assert err <= 1e-2 * float(np.abs(ref).max()) + 1e-6, err
     sub_lse = np.array([f64(lse)[r, h] for r, h in samples])
     assert float(np.abs(sub_lse - ref_lse).max()) <= LSE_TOL
+
+
+CHAIN_CASES = {
+    # name: (kv, window, capture in a CUDA graph)
+    "bf16_eager": ("bf16", 0, False),
+    "bf16_graph": ("bf16", 0, True),
+    "bf16_window300": ("bf16", 300, False),
+    "fp8_eager": ("fp8", 0, False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHAIN_CASES))
+def test_layer_chain_with_early_context_loads(name):
+    """Four layers issued back to back as a model issues them, every layer after the first with the
+    context-stable flag (its context tiles load before the previous layer's merge has finished).  Each
+    layer's queries are the previous layer's output buffer, pre-filled with NaN, and one workspace serves
+    every layer, so a query read before the previous merge ends, or partials overwritten while that merge
+    reads them, shows up.  The batch is ragged: an empty context, contexts of one split, several splits.
+    The oracle runs the same chain on its own bf16-rounded outputs."""
+    import oracle
+    import oracle.fp8_oracle as fp8_oracle
+    from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inputs
+
+    kv, window, graph = CHAIN_CASES[name]
+    layers = 4
+    parents = [synth.chain_parents(0), synth.chain_parents(8), _tree(7, 22), synth.chain_parents(5)]
+    w = workload(parents, [0, 100, 2500, 5000], seed=11 + len(name), scale=1.0, layers=layers, kv=kv)
+    d = device_inputs(w)
+    fp8 = kv == "fp8"
+    st = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, layers, max(w.vocab, 1), window=window,
+                    k_scales=w.k_scales if fp8 else None, v_scales=w.v_scales if fp8 else None)
+
+    def chain():
+        for o in st.out:
+            o.fill_(float("nan"))
+        for layer in range(layers):
+            q = w.q[0] if layer == 0 else st.out[layer - 1]
+            st.attention(layer, q, w.k_cache[layer], w.v_cache[layer], w.k_new[layer], w.v_new[layer],
+                         d["page_table"], d["ctx_lens"], d["parents"], ctx_stable=layer > 0)
+
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            chain()   # warm-up outside the capture
+            with torch.cuda.graph(g, stream=s):
+                chain()
+        torch.cuda.current_stream().wait_stream(s)
+        run = g.replay
+    else:
+        run = chain
+
+    q_ref = f64(w.q[0])
+    refs = []
+    for layer in range(layers):
+        args = (w.k_new[layer], w.v_new[layer])
+        if fp8:
+            codes = lambda t: t.detach().cpu().numpy()
+            ref, _ = fp8_oracle.verify_attention_fp8(q_ref, codes(w.k_cache[layer]), codes(w.v_cache[layer]),
+                                                     w.k_scales[layer], w.v_scales[layer], f64(args[0]),
+                                                     f64(args[1]), w.page_table, w.ctx_lens, w.q_indptr, w.parents,
+                                                     window=window or None)
+        else:
+            ref, _ = oracle.verify_attention(q_ref, f64(w.k_cache[layer]), f64(w.v_cache[layer]), f64(args[0]),
+                                             f64(args[1]), w.page_table, w.ctx_lens, w.q_indptr, w.parents,
+                                             window=window or None)
+        refs.append(ref)
+        # the next layer's queries: this layer's output as the kernel stores it (bf16)
+        q_ref = torch.from_numpy(ref).to(torch.bfloat16).to(torch.float64).numpy()
+
+    for _ in range(3):
+        st.dev_status.zero_()
+        run()
+        torch.cuda.synchronize()
+        assert int(st.dev_status.item()) == 0
+        for layer in range(layers):
+            got = f64(st.out[layer])
+            assert np.isfinite(got).all(), layer
+            err = float(np.abs(got - refs[layer]).max())
+            # later layers also carry the previous layers' output rounding in their queries
+            assert err <= attn_bound(refs[layer]), (layer, err, attn_bound(refs[layer]))
