@@ -20,15 +20,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// One 256-thread block per (node row, query head): four groups of 64
-// threads each take every fourth split, thread t of a group owning dims
-// 4t..4t+3 (8 bytes of each partial row).  A thread issues the loads of up to
-// kBatch of its splits before it uses any (one round of memory latency for up
-// to 4 * kBatch splits) and keeps its group's running (max, sum, weighted sum)
-// in base 2; the four groups are combined once, through shared memory.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeGroups = kMergeThreads / 64;
-constexpr int kBatch = 12;
+// One 128-thread block per (node row, query head): four warps each take every
+// fourth split, lane t owning dims 8t..8t+7 (16 bytes of each partial row).  A
+// thread issues the loads of up to kBatch of its splits before it uses any
+// (one round of memory latency for up to 4 * kBatch splits) and keeps its
+// warp's running (max, sum, weighted sum) in base 2; the four warps are
+// combined once, through shared memory.  The blocks are scheduled while the
+// split kernel runs (one warp per scheduler, a few registers each), so several
+// fit beside a resident split CTA and none keeps the next layer's split CTAs
+// off an SM once the current one exits.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeGroups = kMergeThreads / 32;
+constexpr int kBatch = 9;
+
+__device__ __forceinline__ void add_weighted(float (&acc)[8], float wk, const uint4& o) {
+  const float2 a = unpack_bf16(o.x), b = unpack_bf16(o.y), c = unpack_bf16(o.z), d = unpack_bf16(o.w);
+  acc[0] += wk * a.x; acc[1] += wk * a.y; acc[2] += wk * b.x; acc[3] += wk * b.y;
+  acc[4] += wk * c.x; acc[5] += wk * c.y; acc[6] += wk * d.x; acc[7] += wk * d.y;
+}
 
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p, const BatchDesc bd) {
   // The next kernel in the stream (the next layer's split kernel) may be
@@ -53,58 +62,63 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
   if (ns == 1) return;  // written directly by the split kernel
   const size_t stride = (size_t)bd.total_nodes * kHq;   // rows between splits
   const size_t row0 = (size_t)r * kHq + head;
-  __shared__ float4 s_acc[kMergeGroups][64];
+  __shared__ float4 s_acc[kMergeGroups][2][32];
   __shared__ float s_max[kMergeGroups], s_den[kMergeGroups];
-  const int grp = threadIdx.x >> 6, t = threadIdx.x & 63;
+  const int grp = threadIdx.x >> 5, t = threadIdx.x & 31;
   float mx = -INFINITY, den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int base = 0; base < ns; base += kBatch * kMergeGroups) {
     float w[kBatch];
-    uint2 o[kBatch];   // 4 bf16
+    uint4 o[kBatch];   // 8 bf16
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int s = base + grp + k * kMergeGroups;
       const size_t row = (size_t)min(s, ns - 1) * stride + row0;
       w[k] = s < ns ? p.lse_part[row] : -INFINITY;
-      o[k] = reinterpret_cast<const uint2*>(p.o_part + row * kDim)[t];
+      o[k] = reinterpret_cast<const uint4*>(p.o_part + row * kDim)[t];
     }
     float bm = mx;
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, w[k]);
-    if (bm > mx) {   // rescale what this group has so far to the new maximum
+    if (bm > mx) {   // rescale what this warp has so far to the new maximum
       const float a = mx == -INFINITY ? 0.f : fast_exp2(mx - bm);
-      den *= a; acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+      den *= a;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= a;
       mx = bm;
     }
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const float wk = w[k] == -INFINITY ? 0.f : fast_exp2(w[k] - mx);   // padding entries weigh 0
-      const float2 a = unpack_bf16(o[k].x), b = unpack_bf16(o[k].y);
       den += wk;
-      acc.x += wk * a.x; acc.y += wk * a.y; acc.z += wk * b.x; acc.w += wk * b.y;
+      add_weighted(acc, wk, o[k]);
     }
   }
-  s_acc[grp][t] = acc;
+  s_acc[grp][0][t] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  s_acc[grp][1][t] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   if (t == 0) { s_max[grp] = mx; s_den[grp] = den; }
   __syncthreads();
   if (grp > 0) return;
   float m_all = s_max[0];
 #pragma unroll
   for (int k = 1; k < kMergeGroups; ++k) m_all = fmaxf(m_all, s_max[k]);
-  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float d_all = 0.f;
 #pragma unroll
   for (int k = 0; k < kMergeGroups; ++k) {
-    const float a = s_max[k] == -INFINITY ? 0.f : fast_exp2(s_max[k] - m_all);   // a group may hold no split
-    const float4 v = s_acc[k][t];
+    const float a = s_max[k] == -INFINITY ? 0.f : fast_exp2(s_max[k] - m_all);   // a warp may hold no split
+    const float4 v0 = s_acc[k][0][t], v1 = s_acc[k][1][t];
     d_all += a * s_den[k];
-    sum.x += a * v.x; sum.y += a * v.y; sum.z += a * v.z; sum.w += a * v.w;
+    sum[0] += a * v0.x; sum[1] += a * v0.y; sum[2] += a * v0.z; sum[3] += a * v0.w;
+    sum[4] += a * v1.x; sum[5] += a * v1.y; sum[6] += a * v1.z; sum[7] += a * v1.w;
   }
   const float inv = 1.f / d_all;
-  uint2 packed;
-  packed.x = pack_bf16(sum.x * inv, sum.y * inv);
-  packed.y = pack_bf16(sum.z * inv, sum.w * inv);
-  reinterpret_cast<uint2*>(p.out + row0 * kDim)[t] = packed;
+  uint4 packed;
+  packed.x = pack_bf16(sum[0] * inv, sum[1] * inv);
+  packed.y = pack_bf16(sum[2] * inv, sum[3] * inv);
+  packed.z = pack_bf16(sum[4] * inv, sum[5] * inv);
+  packed.w = pack_bf16(sum[6] * inv, sum[7] * inv);
+  reinterpret_cast<uint4*>(p.out + row0 * kDim)[t] = packed;
   if (p.lse != nullptr && t == 0) p.lse[row0] = (m_all + fast_log2(d_all)) * kLn2;
 }
 
