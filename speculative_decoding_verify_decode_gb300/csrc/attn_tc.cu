@@ -29,8 +29,8 @@ bool cache_map(CUtensorMap* map, const void* cache, int pool_pages) {
 }  // namespace
 
 size_t tc_smem_bytes(int nq) {
-  const int natom = (nq + 63) / 64;
-  return (size_t)nq * 512 + 2 * (size_t)kTileB + (size_t)natom * kAtomB + sizeof(Small);
+  // the P^T tile always spans two 64-column atoms: the PV product takes its 128 rows as M
+  return (size_t)nq * 512 + 2 * (size_t)kTileB + 2 * (size_t)kAtomB + sizeof(Small);
 }
 
 TcPlan tc_plan(int max_nodes) {

@@ -13,16 +13,21 @@
 // Layout of the work.  A CTA owns (split s, KV head g, head part c, sequence
 // b): hpc query heads of group g (6, 3, 2 or 1, so that hpc * N <= 96)
 // times the sequence's N draft nodes form NQ (multiple of 16) query columns.
-// Tokens are the MMA's M dimension ("swap-AB"), so a 128-token K/V tile
-// serves every query column at once:
+// For QK the tokens are the MMA's M dimension ("swap-AB"), so a 128-token K
+// tile serves every query column at once; PV then takes the query columns as
+// M (padded to 128) and all 256 dims as N:
 //   S^T[128 tok][NQ]  = K_tile[128 tok][256] . Q^T                (K-major A and B)
-//   O^T[256 dim][NQ] += V_tile^T[256][128 tok] . P^T[128 tok][NQ]  (MN-major A and B)
-//   l[NQ]            += 1^T . P^T                                  (column sums of P)
-// S^T (double-buffered), O^T and l live in tensor memory (5 * NQ <= 480 of
-// the 512 columns).  The column sums are taken by the tensor core from the
-// same bf16 P^T the PV product uses.  When a sequence needs several CTAs for
-// its query heads (hpc < 6), the CTAs of one split are adjacent in launch
-// order and read the same pages while they are still in L2.
+//   O[128 q][256 dim] += P[128 q][128 tok] . V_tile[128 tok][256]  (MN-major A and B)
+// S^T (double-buffered, 2 * NQ columns) and O (256 columns, one query column
+// per tensor-memory lane) live in tensor memory.  P is the bf16 P^T tile the
+// softmax writes, read as an MN-major A operand; its rows past NQ are never
+// written and only reach rows of O that are never read.  The column sums of P
+// (the softmax denominators) are added by the softmax warps from the same
+// rounded P^T tile.  Because a thread of the epilogue holds a whole 512-byte
+// output row, the rows leave tensor memory straight for global memory.  When a
+// sequence needs several CTAs for its query heads (hpc < 6), the CTAs of one
+// split are adjacent in launch order and read the same pages while they are
+// still in L2.
 //
 // Operand tiles (Q^T, K, V) are "block-major": four 64-dim blocks, each
 // holding every row of the tile at 128 B with the 128-byte swizzle, so the
@@ -35,8 +40,8 @@
 // taking QK of tile i and PV of tile i-1 in whichever order their inputs
 // arrive; warps 2-5 (one per tensor-memory lane quarter, thread = token row)
 // run the online softmax: masking, a running per-column maximum that is only
-// raised (and O^T, l rescaled) when a score exceeds it by more than 2^8,
-// exp2, and the bf16 P^T tile.  Every wait on an mbarrier is bounded; on
+// raised (and O, l rescaled) when a score exceeds it by more than 2^8, exp2,
+// and the bf16 P^T tile.  Every wait on an mbarrier is bounded; on
 // expiry the kernel reports SD_DEV_TIMEOUT and winds down.
 //
 // Quantised cache (KV8).  The context K/V pages hold e4m3 codes with one
@@ -122,7 +127,7 @@ static_assert(offsetof(Small, m) % 16 == 0 && offsetof(Small, alpha) % 16 == 0 &
                   offsetof(Small, outrow) % 16 == 0 && offsetof(Small, lo_col) % 16 == 0,
               "per-column arrays must be 16-byte aligned");
 static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
-static_assert(kTcMaxNQ * 512 + 2 * kTileB + (kTcMaxNQ + 63) / 64 * kAtomB + sizeof(Small) <= 232448,
+static_assert(kTcMaxNQ * 512 + 2 * kTileB + 2 * kAtomB + sizeof(Small) <= 232448,
               "the widest tile configuration must fit in 227 KB of shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -371,10 +376,10 @@ __global__ void __launch_bounds__(KV8 ? kThreads8 : kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
   constexpr int NG = (NQ + 31) / 32;          // 32-column groups
-  constexpr int NATOM = (NQ + 63) / 64;       // 64-column atoms of the P^T tile
+  constexpr int NATOM = (NQ + 63) / 64;       // 64-column atoms of the P^T tile the softmax writes
   constexpr int kQB = NQ * 512;               // Q^T tile: 4 blocks of NQ rows x 128 B
   constexpr uint32_t kColS0 = 0, kColO = 2 * NQ;   // tensor-memory columns
-  static_assert(4 * NQ <= 512, "tensor memory holds 2 S^T and 2 O^T halves");
+  static_assert(2 * NQ + kDim <= 512, "tensor memory holds 2 S^T buffers and O");
   // The kernel declares no static shared memory, so the dynamic window starts
   // at a 1024-byte boundary (required by the 128-byte swizzle atoms); indexing
   // it directly keeps every access a shared-space one.
@@ -385,7 +390,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   uint8_t* sK8 = sV + kHalfB;        // quantised cache: two e4m3 K slots
   uint8_t* sV8 = sK8 + 2 * kSlotB;   // quantised cache: two e4m3 V slots
   uint8_t* sP = sK + 2 * kTileB;
-  Small* sm = reinterpret_cast<Small*>(sP + NATOM * kAtomB);
+  Small* sm = reinterpret_cast<Small*>(sP + 2 * kAtomB);   // P^T spans 128 columns: PV takes M = 128
 
   constexpr int NT = KV8 ? kThreads8 : kThreads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -817,7 +822,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescQK = f16_idesc(128, NQ, 0, 0, !KV8);
-      constexpr uint32_t kIdescPV = f16_idesc(128, NQ, 1, 1, !KV8);
+      constexpr uint32_t kIdescPV = f16_idesc(128, kDim, 1, 1, !KV8);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV), p_addr = smem_u32(sP);
       int kf = 0, pf = 0, vf0 = 0, vf1 = 0;
       int pv_half = 0;   // the PV product of a context tile runs in two 64-token halves
@@ -886,20 +891,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
               ++vf1;
             }
             tc_fence_after();
-            // O^T += V^T . P^T over 16-token steps j0 .. j0 + steps - 1 (V rows from step vj0 of the buffer on)
+            // O += P . V over 16-token steps j0 .. j0 + steps - 1 (V rows from step vj0 of the buffer on)
             auto issue_pv = [&](const int j0, const int steps, const int vj0) {
 #pragma unroll
               for (int jj = 0; jj < steps; ++jj) {
                 const int j = j0 + jj;
                 const uint32_t acc = (t > 0 || j > 0) ? 1u : 0u;
-                // B = P^T, MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
-                const uint64_t pb = sw128_desc(p_addr + j * 2048, kAtomB, 1024);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  // A = V^T dims 128h.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
-                  umma(tmem + kColO + h * NQ, sw128_desc(v_addr + h * 2048 + (j - vj0) * 2 * kGroupB, 1024, kGroupB),
-                       pb, kIdescPV, acc);
-                }
+                // A = P (the P^T tile), MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart;
+                // B = V, MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart
+                umma(tmem + kColO, sw128_desc(p_addr + j * 2048, kAtomB, 1024),
+                     sw128_desc(v_addr + (j - vj0) * 2 * kGroupB, 1024, kGroupB), kIdescPV, acc);
               }
             };
             if (draft) {
@@ -1105,29 +1106,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
         }
         if (i > 0) {
-          // O^T holds earlier tiles: wait for the last PV, then rescale its columns
+          // O holds earlier tiles: wait for the last PV, then rescale the rows
+          // (query columns) of this warp's lane quarter, 32 dims at a time
           if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
           pv_waited = true;
           tc_fence_after();
+          if (quarter * 32 < NQ) {   // warp-uniform: the quarter holds query columns
+            const float al = row < NQ ? sm->alpha[row] : 1.f;
 #pragma unroll 1
-          for (int c16 = 0; c16 < 2 * NQ / 16; ++c16) {   // O^T low, O^T high
-            float v[16];
-            const int col = c16 % (NQ / 16) * 16;
-            const uint32_t a = tmem + lane_addr + kColO + c16 * 16;
-            tmem_ld16(a, v);
-            const float4* al = reinterpret_cast<const float4*>(sm->alpha + col);
-            float f[16];
+            for (int c = 0; c < kDim; c += 32) {
+              float v0[16], v1[16];
+              const uint32_t a = tmem + lane_addr + kColO + c;
+              tmem_ld16(a, v0);
+              tmem_ld16(a + 16, v1);
+              tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float4 t = al[k];
-              f[4 * k] = t.x; f[4 * k + 1] = t.y; f[4 * k + 2] = t.z; f[4 * k + 3] = t.w;
+              for (int e = 0; e < 16; ++e) { v0[e] *= al; v1[e] *= al; }
+              tmem_st16(a, v0);
+              tmem_st16(a + 16, v1);
             }
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] *= f[e];
-            tmem_st16(a, v);
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
       }
       // Pass 2: P = exp2(s - m) as the bf16 P^T row of this token.
@@ -1190,11 +1189,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
 
     // ------------------------------------------------------------ epilogue
-    // Each thread owns dims `row` and 128 + `row` of every query column; the
-    // column sums l are the four warps' partial sums, added from shared
-    // memory.  The normalised bf16 rows (the output, or this split's partial
-    // for the merge) are staged in the idle K/V tiles, 256 values per query
-    // column, and leave as 16-byte vector stores.
+    // Thread `row` of the warps whose lane quarter holds query columns owns
+    // query column q = row: its 256 dims sit in one tensor-memory lane, so it
+    // normalises them by the column sum l (the four warps' partial sums, added
+    // from shared memory) and writes the bf16 row (the output, or this split's
+    // partial for the merge) straight to global memory, 16 bytes at a time.
     if (!*(volatile int*)&sm->abort) {
       // add the warp's four row groups (lanes with the same lane % 8), then
       // publish this warp's column sums
@@ -1220,32 +1219,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const bool direct = nsplit == 1;
       const float o_mul = (KV8 && !has_draft) ? p.v_scale : 1.0f;   // a quantised context tile: the V scale
       const size_t part0 = (size_t)s * bd.total_nodes * kHq;
-      const uint32_t t_row = tmem + lane_addr;
-      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sK);
+      uint8_t* gbase = reinterpret_cast<uint8_t*>(direct ? p.out : p.o_part + part0 * kDim);
+      if (quarter * 32 < rows) {   // warp-uniform: the tensor-memory loads are collective
+        const int q = row;
+        const bool mine = q < rows;
+        const float lq = mine ? sm->lsum[0][q] + sm->lsum[1][q] + sm->lsum[2][q] + sm->lsum[3][q] : 0.f;
+        const float inv = lq > 0.f ? __fdividef(o_mul, lq) : 0.f;   // no visible key in this split: 0
+        uint4* dst = reinterpret_cast<uint4*>(gbase + ((size_t)(mine ? sm->outrow[q] : 0) << 9));
+        const uint32_t t_row = tmem + lane_addr + kColO;
 #pragma unroll 1
-      for (int col = 0; col < NQ; col += 16) {
-        float lo[16], hi[16], l[16];
-        tmem_ld16(t_row + kColO + col, lo);
-        tmem_ld16(t_row + kColO + NQ + col, hi);
+        for (int c = 0; c < kDim; c += 32) {
+          float v0[16], v1[16];
+          tmem_ld16(t_row + c, v0);
+          tmem_ld16(t_row + c + 16, v1);
+          tmem_wait_ld();
+          uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float4 a = reinterpret_cast<const float4*>(sm->lsum[0] + col)[k];
-#pragma unroll
-          for (int w = 1; w < 4; ++w) {
-            const float4 b = reinterpret_cast<const float4*>(sm->lsum[w] + col)[k];
-            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(v0[2 * e] * inv, v0[2 * e + 1] * inv);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(v1[2 * e] * inv, v1[2 * e + 1] * inv);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h0);
+            w[8 + e] = *reinterpret_cast<const uint32_t*>(&h1);
           }
-          l[4 * k] = a.x; l[4 * k + 1] = a.y; l[4 * k + 2] = a.z; l[4 * k + 3] = a.w;
-        }
-        tmem_wait_ld();
-        // every column is written (padding columns too: the staging area holds
-        // NQ rows), so the 16 columns stay independent of each other
+          if (mine) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = col + e;
-          const float inv = l[e] > 0.f ? __fdividef(o_mul, l[e]) : 0.f;   // no visible key in this split: 0
-          stage[q * kDim + row] = __float2bfloat16_rn(lo[e] * inv);
-          stage[q * kDim + 128 + row] = __float2bfloat16_rn(hi[e] * inv);
+            for (int k = 0; k < 4; ++k) dst[c / 8 + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          }
         }
       }
       // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
@@ -1256,27 +1255,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
         } else {
           p.lse_part[part0 + sm->outrow[q]] = lse2;
-        }
-      }
-      if (group_sync()) {
-        // 16-byte chunks of the staged 512-byte rows to their output rows, 4 in
-        // flight per thread (the last round repeats the final chunk instead of branching)
-        const int total = rows << 5;
-        uint8_t* gbase = reinterpret_cast<uint8_t*>(direct ? p.out : p.o_part + part0 * kDim);
-        const int t128 = sw * 32 + lane;
-        for (int c0 = t128; c0 - t128 < total; c0 += 4 * 128) {
-          uint4 v[4];
-          int cc[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            cc[u] = min(c0 + u * 128, total - 1);
-            v[u] = *reinterpret_cast<const uint4*>(sK + cc[u] * 16);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const size_t off = ((size_t)sm->outrow[cc[u] >> 5] << 9) + ((cc[u] & 31) << 4);
-            *reinterpret_cast<uint4*>(gbase + off) = v[u];
-          }
         }
       }
     }
