@@ -417,6 +417,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // Then the merge kernel's blocks may be scheduled (they wait for this grid to
   // finish before reading).
   const bool early = p.ctx_stable != 0 && s != 0;
+  if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
+    if (threadIdx.x == 0) report_dep(p.dev_status, SD_DEV_TIMEOUT);
+    return;
+  }
+  // The draft CTA (split 0) runs to the end in every case: it takes its tensor
+  // memory before the wait (no global memory involved).
+  if (s == 0 && warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
   // the producers fetch their TMA descriptor while the rest of the prologue runs
   if (((!KV8 && (warp == kWarpK || warp == kWarpV)) || (KV8 && warp == kWarpLoad)) && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kWarpV ? &tm_v : &tm_k))
@@ -450,10 +460,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int ctx_end = has_draft ? 0 : min(L, ctx_begin + p.chunk);
   const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
   const int head0 = g * kGroup + c * hpc;
-  if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
-    if (threadIdx.x == 0) report_dep(p.dev_status, SD_DEV_TIMEOUT);
-    return;
-  }
 
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
@@ -808,7 +814,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         sm->lo_col[q] = L + d - W + 1;
       }
     }
-    if (warp == kWarpMma && !early) {
+    if (warp == kWarpMma && !early && s != 0) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
@@ -1041,21 +1047,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
       }
       // Scores of 32 columns of this thread's token row, base 2, masked to -inf.
-      auto load_scores = [&](int g32, float (&v)[32]) {
+      constexpr int kStep = NG == 2 ? 2 : 1;
+      auto mask_scale = [&](int g32, const float (&a)[16], const float (&cc)[16], float (&v)[32]) {
         const uint32_t vm = vis_of(vis, g32);
-        float a[16], cc[16];
-        tmem_ld16(s_addr + g32 * 32, a);
-        const bool second = g32 * 32 + 16 < NQ;
-        if (second) tmem_ld16(s_addr + g32 * 32 + 16, cc);
-        tmem_wait_ld();
-        if (!second) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) cc[e] = 0.f;
-        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float raw = e < 16 ? a[e] : cc[e - 16];
           v[e] = ((vm >> e) & 1u) ? raw * qk_mul : -INFINITY;
+        }
+      };
+      // Groups g32 and g32 + 1 under one tensor-memory wait when there are
+      // exactly two (each round trip costs hundreds of cycles; with three the
+      // registers would spill): kStep groups per call.
+      auto load_scores2 = [&](int g32, float (&v0)[32], float (&v1)[32]) {
+        float a0[16], c0[16], a1[16], c1[16];
+        const bool second0 = g32 * 32 + 16 < NQ;
+        const bool has1 = kStep == 2 && g32 + 1 < NG;
+        const bool second1 = (g32 + 1) * 32 + 16 < NQ;
+        tmem_ld16(s_addr + g32 * 32, a0);
+        if (second0) tmem_ld16(s_addr + g32 * 32 + 16, c0);
+        if (has1) {
+          tmem_ld16(s_addr + g32 * 32 + 32, a1);
+          if (second1) tmem_ld16(s_addr + g32 * 32 + 48, c1);
+        }
+        tmem_wait_ld();
+        if (!second0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) c0[e] = 0.f;
+        }
+        mask_scale(g32, a0, c0, v0);
+        if (has1) {
+          if (!second1) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) c1[e] = 0.f;
+          }
+          mask_scale(g32 + 1, a1, c1, v1);
         }
       };
 
@@ -1065,12 +1091,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (i > 0) {
         float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-        for (int g32 = 0; g32 < NG; ++g32) {
-          float v[32], mm[32];
-          load_scores(g32, v);
+        for (int g32 = 0; g32 < NG; g32 += kStep) {
+          float v0[32], v1[32], mm[32];
+          load_scores2(g32, v0, v1);
           load_cols(sm->m, g32 * 32, mm);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v[e] - mm[e]);
+          for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v0[e] - mm[e]);
+          if (kStep == 2) {
+            load_cols(sm->m, g32 * 32 + 32, mm);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dm[e & 3] = fmaxf(dm[e & 3], v1[e] - mm[e]);
+          }
         }
         const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
         if (lane == 0) sm->flag[i & 1][sw] = 0;
@@ -1083,11 +1114,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (slow) {
         // exact column maxima of this tile, new running maxima and rescale factors
 #pragma unroll 1
-        for (int g32 = 0; g32 < NG; ++g32) {
-          float v[32];
-          load_scores(g32, v);
-          const float mx = transpose_max32(v, lane);
-          sm->red[sw][g32 * 32 + lane] = mx;
+        for (int g32 = 0; g32 < NG; g32 += kStep) {
+          float v0[32], v1[32];
+          load_scores2(g32, v0, v1);
+          sm->red[sw][g32 * 32 + lane] = transpose_max32(v0, lane);
+          if (kStep == 2) sm->red[sw][g32 * 32 + 32 + lane] = transpose_max32(v1, lane);
         }
         if (!group_sync()) break;
         for (int q = sw * 32 + lane; q < NQ; q += 128) {
@@ -1133,10 +1164,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (i > 0 && !pv_waited) {
         if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
       }
-#pragma unroll 1
-      for (int g32 = 0; g32 < NG; ++g32) {
-        float v[32], mm[32];
-        load_scores(g32, v);
+      auto write_p = [&](int g32, const float (&v)[32]) {
+        float mm[32];
         load_cols(sm->m, g32 * 32, mm);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1159,6 +1188,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             *reinterpret_cast<uint4*>(sP + (ch >> 3) * kAtomB + p_off(row, ch & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+      };
+#pragma unroll 1
+      for (int g32 = 0; g32 < NG; g32 += kStep) {
+        float v0[32], v1[32];
+        load_scores2(g32, v0, v1);
+        write_p(g32, v0);
+        if (kStep == 2) write_p(g32 + 1, v1);
       }
       tc_fence_before();
       __syncwarp();
@@ -1225,26 +1261,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const bool mine = q < rows;
         const float lq = mine ? sm->lsum[0][q] + sm->lsum[1][q] + sm->lsum[2][q] + sm->lsum[3][q] : 0.f;
         const float inv = lq > 0.f ? __fdividef(o_mul, lq) : 0.f;   // no visible key in this split: 0
-        uint4* dst = reinterpret_cast<uint4*>(gbase + ((size_t)(mine ? sm->outrow[q] : 0) << 9));
+        // The warp's 32 rows are staged in the idle K tile (16 KB per warp): the
+        // 16-byte chunk ch of the lane's row at chunk ch ^ lane of its 512-byte
+        // slot, so that both the per-lane writes and the per-row reads below
+        // are free of bank conflicts.  Each row then leaves as one coalesced
+        // 512-byte warp store instead of 32 scattered 16-byte ones.
+        uint8_t* wst = sK + quarter * (32 * 512);
         const uint32_t t_row = tmem + lane_addr + kColO;
+        // 128 dims per wait: each tensor-memory round trip costs hundreds of cycles
 #pragma unroll 1
-        for (int c = 0; c < kDim; c += 32) {
-          float v0[16], v1[16];
-          tmem_ld16(t_row + c, v0);
-          tmem_ld16(t_row + c + 16, v1);
+        for (int c = 0; c < kDim; c += 128) {
+          float v[8][16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) tmem_ld16(t_row + c + 16 * k, v[k]);
           tmem_wait_ld();
-          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(v0[2 * e] * inv, v0[2 * e + 1] * inv);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(v1[2 * e] * inv, v1[2 * e + 1] * inv);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h0);
-            w[8 + e] = *reinterpret_cast<const uint32_t*>(&h1);
-          }
-          if (mine) {
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) dst[c / 8 + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            for (int e = 0; e < 8; ++e) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(v[k][2 * e] * inv, v[k][2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            const int ch = (c + 16 * k) / 8;   // 16-byte chunk of the row (8 dims)
+            *reinterpret_cast<uint4*>(wst + lane * 512 + ((ch ^ lane) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(wst + lane * 512 + (((ch + 1) ^ lane) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
           }
+        }
+        __syncwarp();
+        // eight rows per round, their loads issued before any store; the last
+        // round repeats the final row (the same bytes to the same place)
+        const int nrow = min(32, rows - quarter * 32);
+        const int my_out = mine ? sm->outrow[q] : 0;
+#pragma unroll 1
+        for (int r0 = 0; r0 < nrow; r0 += 8) {
+          uint4 val[8];
+          int orow[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = min(r0 + u, nrow - 1);
+            val[u] = *reinterpret_cast<const uint4*>(wst + r * 512 + ((lane ^ r) << 4));
+            orow[u] = __shfl_sync(0xffffffffu, my_out, r);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(gbase + ((size_t)orow[u] << 9) + (lane << 4)) = val[u];
         }
       }
       // log-sum-exp of query column sw * 32 + lane (base 2 for the merge)
