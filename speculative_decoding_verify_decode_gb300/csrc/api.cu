@@ -333,7 +333,7 @@ sd_status sd_sample_accept(int batch, const int* q_indptr_h, int vocab, float te
     return SD_ERR_INVALID_ARG;
   if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.0f / temperature))
     return SD_ERR_INVALID_ARG;
-  if ((long long)vocab > (long long)kSampleMaxTiles * 1024) return SD_ERR_UNSUPPORTED;
+  if ((long long)vocab > (long long)kSampleMaxTiles * kSampleTile) return SD_ERR_UNSUPPORTED;
   const size_t need = sd_sample_accept_workspace_size(batch, q_indptr_h, vocab);
   if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return SD_ERR_WORKSPACE;
   SampleParams p;

@@ -41,8 +41,8 @@ constexpr int kAcceptChunk = 4096;
 cudaError_t launch_accept(const AcceptParams& p, const BatchDesc& bd, cudaStream_t st);
 
 // Sampling-based verify: per-chunk softmax statistics, then one CTA per sequence walking its tree.
-constexpr int kSampleTile = 1024;        // logits per tile of the statistics pass and of the inverse-CDF search
-constexpr int kSampleMaxTiles = 2048;   // vocabulary <= 2048 x 1024
+constexpr int kSampleTile = 4096;        // logits per tile of the statistics pass and of the inverse-CDF search
+constexpr int kSampleMaxTiles = 512;    // vocabulary <= 512 x 4096 = 2048 x 1024
 struct SampleParams {
   const float* logits;        // [sumN][V] target logits
   const float* draft_probs;   // [sumN][V] draft distribution at each node (its children were drawn from it)
