@@ -2,6 +2,8 @@
 // kernels.  Internal to the library (the public interface is sd_verify.h).
 #pragma once
 
+#include <utility>
+
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -59,6 +61,31 @@ struct AttnParams {
   float k_scale;
   float v_scale;
 };
+
+// Programmatic dependent launch of a kernel whose first statement is
+// pdl_wait(): it may be scheduled while the previous kernel in the stream
+// runs, and reads or writes nothing before that kernel has finished.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+// Wait for the previous kernel in the stream (and see its writes), then let
+// the next one be scheduled.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void report(int* status, int bits) {
   if (status != nullptr) atomicOr(status, bits);

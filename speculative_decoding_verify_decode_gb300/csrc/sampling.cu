@@ -56,6 +56,7 @@ __device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float c) {
 
 template <bool kVec4>
 __global__ void __launch_bounds__(256) lse_chunk_kernel(const SampleParams p) {
+  pdl_wait();
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const float* x = p.logits + (size_t)row * p.vocab;
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(256) lse_chunk_kernel(const SampleParams p) {
 // bonus tile sums without a pass of its own.
 template <bool kVec4>
 __global__ void __launch_bounds__(256) resid_tile_kernel(const SampleParams p) {
+  pdl_wait();
   const int row = blockIdx.y, tile = blockIdx.x;
   const float c = p.inv_t * kLog2e;
   __shared__ float s_stat[2];
@@ -209,6 +211,7 @@ __device__ __forceinline__ float block_incl_scan(float v, float* w, float& total
 // kVec4: V % 4 == 0 and 16-byte aligned rows, so passes move four tokens per 16-byte load.
 template <bool kVec4>
 __global__ void __launch_bounds__(kSampleThreads, 1) sample_accept_kernel(const SampleParams p, const BatchDesc bd) {
+  pdl_wait();
   const int b = blockIdx.x;
   const int q0 = bd.q_indptr[b];
   const int n = bd.q_indptr[b + 1] - q0;
@@ -491,18 +494,16 @@ __global__ void __launch_bounds__(kSampleThreads, 1) sample_accept_kernel(const 
 cudaError_t launch_sample_accept(const SampleParams& p, const BatchDesc& bd, cudaStream_t st) {
   dim3 grid(p.chunks, bd.total_nodes);
   const bool aligned = (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
-  if (p.vocab % 4 == 0 && aligned) lse_chunk_kernel<true><<<grid, 256, 0, st>>>(p);
-  else lse_chunk_kernel<false><<<grid, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // each kernel starts by waiting for the one before (pdl_wait): the three run as programmatic dependents
+  cudaError_t e = (p.vocab % 4 == 0 && aligned) ? launch_pdl(lse_chunk_kernel<true>, grid, dim3(256), 0, st, p)
+                                                : launch_pdl(lse_chunk_kernel<false>, grid, dim3(256), 0, st, p);
   if (e != cudaSuccess) return e;
   const bool vec = p.vocab % 4 == 0 && aligned && (reinterpret_cast<uintptr_t>(p.draft_probs) & 15) == 0;
-  if (vec) resid_tile_kernel<true><<<grid, 256, 0, st>>>(p);
-  else resid_tile_kernel<false><<<grid, 256, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = vec ? launch_pdl(resid_tile_kernel<true>, grid, dim3(256), 0, st, p)
+          : launch_pdl(resid_tile_kernel<false>, grid, dim3(256), 0, st, p);
   if (e != cudaSuccess) return e;
-  if (vec) sample_accept_kernel<true><<<bd.batch, kSampleThreads, 0, st>>>(p, bd);
-  else sample_accept_kernel<false><<<bd.batch, kSampleThreads, 0, st>>>(p, bd);
-  return cudaGetLastError();
+  return vec ? launch_pdl(sample_accept_kernel<true>, dim3(bd.batch), dim3(kSampleThreads), 0, st, p, bd)
+             : launch_pdl(sample_accept_kernel<false>, dim3(bd.batch), dim3(kSampleThreads), 0, st, p, bd);
 }
 
 }  // namespace sdv
