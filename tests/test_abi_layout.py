@@ -44,3 +44,16 @@ def test_ctypes_mirror_matches_the_header(tmp_path, struct, header, cls):
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
     assert got[0] == ctypes.sizeof(cls)
     assert got[1:] == [getattr(cls, n).offset for n in names]
+
+
+def test_with_ctx_stable_sets_only_the_flag():
+    base = native.Shape([0, 9, 32], max_pages_per_seq=300, num_pool_pages=700, num_splits=5, window=2048)
+    stable = base.with_ctx_stable()
+    names = [f[0] for f in native.SdShape._fields_]
+    for n in names:
+        if n in ("q_indptr_h", "ctx_stable"):
+            continue
+        assert getattr(stable.c, n) == getattr(base.c, n), n
+    assert list(stable.indptr) == list(base.indptr)
+    assert base.c.ctx_stable == 0 and stable.c.ctx_stable == 1
+    assert stable.with_ctx_stable(False).c.ctx_stable == 0
