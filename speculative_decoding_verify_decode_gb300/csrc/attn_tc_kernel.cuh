@@ -948,7 +948,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // scores to base-2 softmax units; a quantised context tile carries the K scale
     const float qk_mul = (KV8 && !has_draft) ? kScaleLog2 * p.k_scale : kScaleLog2;
     const int quarter = warp & 3;            // tensor-memory lane quarter of this warp
-    const int row = quarter * 32 + lane;     // token row of S^T / dim row of O^T
+    const int row = quarter * 32 + lane;     // token row of S^T; query column (row of O) in the epilogue
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     // Barrier of the four softmax warps on an mbarrier, so that it is bounded too.
     int gphase = 0;
