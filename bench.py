@@ -2,9 +2,11 @@
 
 A step is one pass of the whole hot path over one synthetic batch: verify
 attention for every layer, argmax + greedy accept, and the KV commit of all
-layers.  The default workload is the 8-draft chain verify at 4096 tokens of
-context (16 layers, 24/4 heads, d = 256, bf16 paged KV with a permuted page
-table, logits [9, 151936]); ``--config`` picks another one.
+layers.  The default workload is the long-context tree verify: a 22-node draft
+tree at 131072 tokens of context (16 layers, 24/4 heads, d = 256, bf16 paged KV
+with a permuted page table, logits [23, 151936]); ``--config`` picks another
+one.  The other four workloads of the set are timed after it, more briefly,
+and reported under ``workloads`` (``--no-extra`` skips them).
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
 baseline arm), on a bounded sample of the same workload.
@@ -32,9 +34,11 @@ from speculative_decoding_verify_decode_gb300 import native, synth  # noqa: E402
 from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inputs  # noqa: E402
 
 METRIC = "verify steps/s"
-DEFAULT_CONFIG = "chain8_ctx4k"
+DEFAULT_CONFIG = "ddtree22_ctx128k"
+EXTRA_CONFIGS = ["tiny_chain_ctx512", "chain8_ctx4k", "ddtree22_ctx32k", "conc8_chain4_ragged"]
 ATTN_SRCS = [os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", f)
-             for f in ("attn_tc_kernel.cuh", "attn_tc.cu", "attn_tc8.cu")]
+             for f in ("attn_ring_kernel.cuh", "attn_ring_launch.cuh", "attn_ring.cu", "tc_ptx.cuh",
+                       "attn_tc_kernel.cuh", "attn_tc8.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
 
 
@@ -335,44 +339,47 @@ def time_sample_accept(dev, stream, w, reps: int, temperature: float = 1.0) -> d
             "alg_bytes": alg, "gbs": alg / (us * 1e-6) / 1e9, "frac": alg / (us * 1e-6) / 1e9 / peak, "launches": 3}
 
 
-def run_ours(args, world, rank, local):
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    native.load()
-    w = synth.make_workload(args.config, device=dev, layers=args.layers or None)
+def measure(config: str, dev, stream, steps: int, warmup: int, world: int, splits: int = 0, layers=None,
+            clocks_index=None) -> dict:
+    """Time one workload: the whole step (a CUDA graph replayed `steps` times between events), every
+    layer's verify attention alone (the dominant kernel), and the step end to end with host inputs and
+    results.  Returns the numbers and the objects the headline line reuses."""
+    w = synth.make_workload(config, device=dev, layers=layers)
     d = device_inputs(w, dev)
     fp8 = w.kv == "fp8"
     step = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, w.layers, w.vocab, device=dev,
-                      num_splits=args.splits, window=w.window, k_scales=w.k_scales if fp8 else None,
+                      num_splits=splits, window=w.window, k_scales=w.k_scales if fp8 else None,
                       v_scales=w.v_scales if fp8 else None)
     run_args = (w.q, w.k_cache, w.v_cache, w.k_new, w.v_new, d["page_table"], d["ctx_lens"], d["parents"],
                 d["draft_tokens"], w.logits)
     step.run(*run_args)                       # eager once: surfaces launch errors early
     torch.cuda.synchronize(dev)
     graph = step.capture(*run_args)
-    stream = torch.cuda.current_stream(dev)
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         graph.replay()
     torch.cuda.synchronize(dev)
     status = int(step.dev_status.item())
     if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
+        raise RuntimeError(f"{config}: device status {status} after warm-up")
     accepted = int(step.accept_len.sum().item())
 
-    # ---- timed region: K steps, graph replays back to back
+    # ---- timed region: `steps` steps, graph replays back to back
     barrier(world)
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
+    clk = ClockSampler(clocks_index) if clocks_index is not None else None
+    if clk is not None:
+        clk.__enter__()
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if clk is not None:
+        clk.__exit__(None, None, None)
     barrier(world)
-    ms = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms, world, dev)
-    ms_per_step = ms / args.steps
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms_per_step = ms / steps
 
     # ---- the dominant kernel: every layer's verify attention captured in one
     # graph, replayed between events on the launching stream
@@ -388,7 +395,7 @@ def run_ours(args, world, rank, local):
     stream.wait_stream(cap)
     for _ in range(3):
         attn_graph.replay()
-    reps = max(5, args.steps // 2)
+    reps = max(5, steps // 2)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
     for _ in range(reps):
@@ -410,13 +417,13 @@ def run_ours(args, world, rank, local):
 
     def layout(ts):
         offs, at = [], 0
-        for t in ts:
+        for x in ts:
             offs.append(at)
-            at += (t.numel() * t.element_size() + 255) // 256 * 256
+            at += (x.numel() * x.element_size() + 255) // 256 * 256
         return offs, at
 
     def views(buf, ts, offs):
-        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ts, offs)]
+        return [buf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape) for x, o in zip(ts, offs)]
 
     in_offs, in_bytes = layout(in_list)
     out_offs, out_bytes = layout(out_list)
@@ -425,8 +432,8 @@ def run_ours(args, world, rank, local):
     dev_out_buf = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
     host_out_buf = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     dev_in = views(dev_in_buf, in_list, in_offs)
-    for hv, t in zip(views(host_in_buf, in_list, in_offs), in_list):
-        hv.copy_(t.detach().to("cpu"))
+    for hv, x in zip(views(host_in_buf, in_list, in_offs), in_list):
+        hv.copy_(x.detach().to("cpu"))
     dev_out = views(dev_out_buf, out_list, out_offs)
     L = w.layers
     e2e_args = (dev_in[0:L], w.k_cache, w.v_cache, dev_in[L:2 * L], dev_in[2 * L:3 * L], d["page_table"],
@@ -444,9 +451,7 @@ def run_ours(args, world, rank, local):
                 v.copy_(o)
             host_out_buf.copy_(dev_out_buf, non_blocking=True)
     stream.wait_stream(cap)
-    h2d = in_bytes
-    d2h = out_bytes
-    e2e_steps = max(5, args.steps // 2)
+    e2e_steps = max(5, steps // 2)
     for _ in range(3):
         e2e_graph.replay()
     barrier(world)
@@ -458,7 +463,44 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    if int(step.dev_status.item()) != 0:
+        raise RuntimeError(f"{config}: device status {int(step.dev_status.item())} after the timed runs")
+    return {"w": w, "step": step, "fp8": fp8, "ms_per_step": ms_per_step, "accepted": accepted,
+            "attn_ms": attn_ms, "alg": alg, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+            "e2e_ms": e2e_ms, "h2d": in_bytes, "d2h": out_bytes, "clocks": clk.summary() if clk else None}
 
+
+def config_of(name: str, w, world: int) -> dict:
+    """The workload-defining keys of `config`, the same in both arms."""
+    per_step = attn_bytes_per_layer(w) * w.layers
+    return {"workload": name, "batch": w.batch, "layers": w.layers, "window": w.window, "kv": w.kv,
+            "ctx_lens": [int(x) for x in w.ctx_lens][:8], "draft_nodes": w.total_nodes, "vocab": w.vocab,
+            "heads": "24q/4kv", "head_dim": 256, "page": 16,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": (f"inputs larger than L2 (KV read per step {per_step / 1e6:.0f} MB > 129 MB)" if per_step > 129e6
+                   else f"inputs smaller than L2 (KV read per step {per_step / 1e6:.1f} MB): warm-cache figure")}
+
+
+def workload_summary(m: dict, world: int) -> dict:
+    """The numbers of one workload, as reported under `workloads`."""
+    return {"value": world * 1000.0 / m["ms_per_step"], "unit": "steps/s", "ms_per_step": m["ms_per_step"],
+            "l2": config_of("", m["w"], world)["l2"],
+            "accepted_tok_per_s": world * m["accepted"] * 1000.0 / m["ms_per_step"],
+            "attn_us_per_layer": m["attn_ms"] * 1000.0, "kv_read_gbs": m["achieved"],
+            "frac": m["achieved"] / m["peak"],
+            "e2e": {"value": world * 1000.0 / m["e2e_ms"], "unit": "steps/s", "h2d_bytes_per_step": m["h2d"],
+                    "d2h_bytes_per_step": m["d2h"]}}
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    native.load()
+    stream = torch.cuda.current_stream(dev)
+    m = measure(args.config, dev, stream, args.steps, args.warmup, world, splits=args.splits,
+                layers=args.layers or None, clocks_index=local)
+    w, step = m["w"], m["step"]
+    ms_per_step = m["ms_per_step"]
     line = {
         "metric": METRIC,
         "value": world * 1000.0 / ms_per_step,
@@ -470,27 +512,23 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16",
+        "dtype": "e4m3 KV, f16 MMA" if m["fp8"] else "bf16",
         "data": ("synthetic (seeded; Q and draft K/V ~ N(0,1)/16 bf16, random e4m3 cache codes with per-layer "
-                 "scales, planted-argmax fp32 logits)" if fp8 else
+                 "scales, planted-argmax fp32 logits)" if m["fp8"] else
                  "synthetic (seeded; Q/K/V ~ N(0,1)/16 bf16, planted-argmax fp32 logits)"),
-        "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "window": w.window, "kv": w.kv,
-                   "ctx_lens": [int(x) for x in w.ctx_lens][:8], "draft_nodes": w.total_nodes,
-                   "vocab": w.vocab, "heads": "24q/4kv", "head_dim": 256, "page": 16,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (KV read per step exceeds 129 MB)",
-                   "cuda_graph": True},
-        "accepted_tokens_per_step": accepted,
-        "accepted_tok_per_s": world * accepted * 1000.0 / ms_per_step,
-        "kv_read_gbs": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_for(args.config),
+        "config": config_of(args.config, w, world),
+        "cuda_graph": True,
+        "accepted_tokens_per_step": m["accepted"],
+        "accepted_tok_per_s": world * m["accepted"] * 1000.0 / ms_per_step,
+        "kv_read_gbs": m["achieved"],
+        "roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": m["peak"], "unit": "GB/s",
+                     "frac": m["achieved"] / m["peak"], "traffic": traffic_for(args.config),
                      "kernel": "verify attention of one layer (split kernel + merge), from a graph of all layers",
-                     "alg_bytes_per_launch": alg, "launch_ms": attn_ms, "peak_kind": peak_kind},
-        "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                     "alg_bytes_per_launch": m["alg"], "launch_ms": m["attn_ms"], "peak_kind": m["peak_kind"]},
+        "e2e": {"value": world * 1000.0 / m["e2e_ms"], "unit": "steps/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"]},
         "gpu_launches": step.launches_per_step() * args.steps,
-        "clocks": clk.summary(),
+        "clocks": m["clocks"],
     }
     if args.config.startswith("ddtree"):
         line["ddtree_build"] = time_ddtree_build(dev, stream, w.batch, w.total_nodes // w.batch - 1)
@@ -498,72 +536,107 @@ def run_ours(args, world, rank, local):
         line["gdn_layers"] = time_gdn(dev, stream, w, reps=max(5, args.steps // 2))
     line["sample_accept"] = time_sample_accept(dev, stream, w, reps=max(5, args.steps // 2))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.config, reps=1)
+        line["cpu_baseline"] = cpu_baseline(w, args.config, reps=3)
+    del m, w, step
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        # the other workloads of the set, each timed the same way over fewer steps
+        extra = {}
+        for cfg in EXTRA_CONFIGS:
+            if cfg == args.config:
+                continue
+            mx = measure(cfg, dev, stream, max(10, args.steps // 2), 3, world, splits=args.splits)
+            extra[cfg] = workload_summary(mx, world)
+            del mx
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
     return line
 
 
 # ---------------------------------------------------------------- CPU oracle arm
 
-def cpu_baseline(w, config: str, reps: int = 1) -> dict:
-    """Time the oracle on a bounded sample: one layer's attention + accept + commit.
-
-    A step is extrapolated as layers x attention + accept + commit.
-    """
+def _oracle_sample(w, host, logits):
+    """One sample of the oracle: one layer's attention, the accept, one layer's commit (seconds each)."""
     import oracle
     import oracle.fp8_oracle as fp8_oracle
-    f32 = lambda t: t.detach().to("cpu", torch.float32).numpy()
     layer = 0
     fp8 = w.kv == "fp8"
-    cache = (lambda t: t.detach().cpu().numpy()) if fp8 else f32
-    host = dict(q=f32(w.q[layer]), kc=cache(w.k_cache[layer]), vc=cache(w.v_cache[layer]),
-                kn=f32(w.k_new[layer]), vn=f32(w.v_new[layer]))
-    logits = w.logits.detach().cpu().numpy()
-    t_attn, t_acc, t_com = [], [], []
-    for _ in range(reps):
-        t = time.perf_counter()
-        if fp8:
-            fp8_oracle.verify_attention_fp8(host["q"], host["kc"], host["vc"], w.k_scales[layer], w.v_scales[layer],
-                                            host["kn"], host["vn"], w.page_table, w.ctx_lens, w.q_indptr,
-                                            w.parents, window=w.window or None)
-        else:
-            oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
-                                    w.ctx_lens, w.q_indptr, w.parents, window=w.window or None)
-        t_attn.append(time.perf_counter() - t)
-        t = time.perf_counter()
-        _, lens, paths, _ = oracle.accept(w.q_indptr, w.parents, w.draft_tokens, logits)
-        t_acc.append(time.perf_counter() - t)
-        t = time.perf_counter()
-        if fp8:
-            fp8_oracle.kv_commit_fp8([host["kc"]], [host["vc"]], [w.k_scales[layer]], [w.v_scales[layer]],
-                                     [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens, w.q_indptr, lens, paths)
-        else:
-            oracle.kv_commit([host["kc"]], [host["vc"]], [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens,
-                             w.q_indptr, lens, paths)
-        t_com.append(time.perf_counter() - t)
-    step_s = w.layers * statistics.mean(t_attn) + statistics.mean(t_acc) + w.layers * statistics.mean(t_com)
+    t = time.perf_counter()
+    if fp8:
+        fp8_oracle.verify_attention_fp8(host["q"], host["kc"], host["vc"], w.k_scales[layer], w.v_scales[layer],
+                                        host["kn"], host["vn"], w.page_table, w.ctx_lens, w.q_indptr,
+                                        w.parents, window=w.window or None)
+    else:
+        oracle.verify_attention(host["q"], host["kc"], host["vc"], host["kn"], host["vn"], w.page_table,
+                                w.ctx_lens, w.q_indptr, w.parents, window=w.window or None)
+    t_attn = time.perf_counter() - t
+    t = time.perf_counter()
+    _, lens, paths, _ = oracle.accept(w.q_indptr, w.parents, w.draft_tokens, logits)
+    t_acc = time.perf_counter() - t
+    t = time.perf_counter()
+    if fp8:
+        fp8_oracle.kv_commit_fp8([host["kc"]], [host["vc"]], [w.k_scales[layer]], [w.v_scales[layer]],
+                                 [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens, w.q_indptr, lens, paths)
+    else:
+        oracle.kv_commit([host["kc"]], [host["vc"]], [host["kn"]], [host["vn"]], w.page_table, w.ctx_lens,
+                         w.q_indptr, lens, paths)
+    t_com = time.perf_counter() - t
+    return t_attn, t_acc, t_com
+
+
+def _host_copies(w):
+    f32 = lambda x: x.detach().to("cpu", torch.float32).numpy()
+    fp8 = w.kv == "fp8"
+    cache = (lambda x: x.detach().cpu().numpy()) if fp8 else f32
+    host = dict(q=f32(w.q[0]), kc=cache(w.k_cache[0]), vc=cache(w.v_cache[0]), kn=f32(w.k_new[0]),
+                vn=f32(w.v_new[0]))
+    return host, w.logits.detach().cpu().numpy()
+
+
+def cpu_baseline(w, config: str, reps: int = 3) -> dict:
+    """Time the oracle on a bounded sample: `reps` repetitions of one layer's attention + accept + one
+    layer's commit; the median of each part is extrapolated to a step of `w.layers` layers."""
+    host, logits = _host_copies(w)
+    parts = [_oracle_sample(w, host, logits) for _ in range(reps)]
+    t_attn = statistics.median(p[0] for p in parts)
+    t_acc = statistics.median(p[1] for p in parts)
+    t_com = statistics.median(p[2] for p in parts)
+    step_s = w.layers * t_attn + t_acc + w.layers * t_com
     return {"value": 1.0 / step_s, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{config}: {reps} x (1 layer attention + accept + 1 layer commit) on the host, "
+            "sample": f"{config}: median of {reps} x (1 layer attention + accept + 1 layer commit) on the host, "
                       f"extrapolated to {w.layers} layers; numpy fp64",
-            "attn_s_per_layer": statistics.mean(t_attn), "accept_s": statistics.mean(t_acc)}
+            "reps": reps, "layers_extrapolated": w.layers,
+            "attn_s_per_layer": t_attn, "accept_s": t_acc, "commit_s_per_layer": t_com}
 
 
 def run_reference(args, world, rank, local):
+    """The oracle arm: `warmup` untimed and `steps` timed samples, each one layer's attention + accept + one
+    layer's commit.  `ms_per_step` is the measured time of one sample (so steps x ms_per_step is the timed
+    wall time); `value` extrapolates the median sample to a whole step of the workload's layers."""
     if rank != 0:
         return None
-    dev = "cpu"
-    w = synth.make_workload(args.config, device=dev)
-    reps = max(1, args.steps)
-    base = cpu_baseline(w, args.config, reps=1)          # warm-up sample
+    w = synth.make_workload(args.config, device="cpu")
+    host, logits = _host_copies(w)
+    for _ in range(args.warmup):
+        _oracle_sample(w, host, logits)
     t = time.perf_counter()
-    base = cpu_baseline(w, args.config, reps=reps)
+    parts = [_oracle_sample(w, host, logits) for _ in range(max(1, args.steps))]
     wall = time.perf_counter() - t
-    v = base["value"]
-    return {"metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": args.config, "batch": w.batch, "layers": w.layers, "vocab": w.vocab,
-                       "window": w.window, "kv": w.kv},
-            "impl": "reference", "cpu_baseline": {**base, "wall_s": wall},
+    t_attn = statistics.median(p[0] for p in parts)
+    t_acc = statistics.median(p[1] for p in parts)
+    t_com = statistics.median(p[2] for p in parts)
+    v = 1.0 / (w.layers * t_attn + t_acc + w.layers * t_com)
+    base = {"value": v, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{args.config}: each timed step is 1 layer attention + accept + 1 layer commit on the host "
+                      f"(numpy fp64); value extrapolates the median step to {w.layers} layers",
+            "reps": len(parts), "layers_extrapolated": w.layers, "wall_s": wall,
+            "attn_s_per_layer": t_attn, "accept_s": t_acc, "commit_s_per_layer": t_com}
+    return {"metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": len(parts),
+            "warmup": args.warmup, "ms_per_step": 1000.0 * wall / len(parts), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_of(args.config, w, world),
+            "impl": "reference", "timed_step": "1 layer attention + accept + 1 layer commit",
+            "layers_extrapolated": w.layers, "cpu_baseline": base,
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -576,6 +649,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gdn", action="store_true", help="skip the hybrid (Gated DeltaNet) layers' timing")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads of the set")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload to build (0 = its own count; fewer only for profiler captures)")
     ap.add_argument("--splits", type=int, default=0, help="split-KV chunks per (sequence, KV head); 0 = auto")

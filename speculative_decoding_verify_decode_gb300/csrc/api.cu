@@ -58,13 +58,15 @@ struct SplitPlan {
   int nsplit;    // splits in the grid: the draft split + the context splits
 };
 
-// Context tokens per context split.  Every split CTA (one per SM) pays a fixed
-// set-up and epilogue, so a single sequence gets one wave of CTAs, each with
-// an equal share of the 128-token tiles; a batch, whose context lengths are
-// not known on the host, is cut for two waves of the worst case (every
-// sequence full), which keeps the last wave short when the lengths are ragged.
-SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
-  const int tile = attn_tc_tile();
+// Context tokens per context split, for a kernel that runs `hparts` CTAs per
+// (split, sequence, KV head).  Every split CTA (one per SM) pays a fixed set-up
+// and epilogue, so a single sequence gets one wave of CTAs, each with an equal
+// share of the 128-token tiles; a batch, whose context lengths are not known on
+// the host, is cut for two waves of the worst case (every sequence full), which
+// keeps the last wave short when the lengths are ragged.  num_splits > 0 fixes
+// the number of context chunks per (sequence, KV head) instead.
+SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd, int hparts) {
+  const int tile = kTileTokens;
   long long max_ctx = (long long)s->max_pages_per_seq * kPage;
   // with a window only the tiles from window_base on are read: at most W - 1 positions plus the
   // rounding to a tile boundary
@@ -74,7 +76,7 @@ SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
   if (s->num_splits > 0) {
     chunk = (max_ctx + s->num_splits - 1) / s->num_splits;
   } else {
-    const long long streams = (long long)bd.batch * kHkv * tc_plan(bd.max_nodes).hparts;
+    const long long streams = (long long)bd.batch * kHkv * hparts;
     const long long waves = bd.batch > 1 ? 2 : 1;
     long long slots = waves * device_sm_count() - streams;    // the draft CTAs take one slot per stream
     if (slots < streams) slots = streams;
@@ -85,6 +87,11 @@ SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd) {
   if (chunk < tile) chunk = tile;
   const long long n = 1 + (max_ctx + chunk - 1) / chunk;   // the draft split + the context chunks
   return SplitPlan{(int)chunk, (int)n};
+}
+
+// The plan of each cache kind: bf16 caches run the ring kernel, e4m3 caches the converter kernel.
+SplitPlan plan_for(const sd_shape* s, const BatchDesc& bd, bool fp8) {
+  return plan_splits(s, bd, fp8 ? tc_plan(bd.max_nodes).hparts : ring_plan(bd.max_nodes).hparts);
 }
 
 size_t attn_workspace(const SplitPlan& pl, const BatchDesc& bd) {
@@ -138,7 +145,7 @@ sd_status verify_attn(const sd_shape* shape, const void* q, const void* k_cache,
       !aligned16(out) || (workspace != nullptr && !aligned16(workspace)))
     return SD_ERR_INVALID_ARG;
   if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return SD_ERR_INVALID_ARG;
-  const SplitPlan pl = plan_splits(shape, bd);
+  const SplitPlan pl = plan_for(shape, bd, fp8);
   const size_t need = attn_workspace(pl, bd);
   if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SD_ERR_WORKSPACE;
 
@@ -242,7 +249,9 @@ const char* sd_status_string(sd_status s) {
 size_t sd_verify_attn_workspace_size(const sd_shape* shape) {
   BatchDesc bd;
   if (check_shape(shape, &bd) != SD_OK) return 0;
-  return attn_workspace(plan_splits(shape, bd), bd);
+  // one size serves both cache kinds (sd_verify_attn and sd_verify_attn_fp8 share the query)
+  const size_t a = attn_workspace(plan_for(shape, bd, false), bd), b = attn_workspace(plan_for(shape, bd, true), bd);
+  return a > b ? a : b;
 }
 
 sd_status sd_verify_attn(const sd_shape* shape, const void* q, const void* k_cache, const void* v_cache,

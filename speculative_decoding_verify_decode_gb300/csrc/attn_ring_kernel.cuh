@@ -1,0 +1,880 @@
+// Split-KV verify attention over bf16 pages, one CTA per (split, KV head):
+// every query head of the KV group in one tile, K and V streamed through
+// fine-grained shared-memory rings, accumulators in tensor memory (tcgen05).
+//
+// What it computes is the tree/causal-masked grouped-query attention of the
+// verify step: for sequence b, draft node j and query head h, softmax
+// attention (scale 1/16) of q[j][h] over every context token of KV head h/6
+// plus the draft nodes on j's root path.  Sources, by page title:
+// «如何在单张 RTX 3090 上让 Qwen3.5-27B token 生成速度提升 6 倍» (为什么我们要做这个测试:
+// 24 Q / 4 KV heads, head dim 256; 关键突破: the tree mask follows each node's
+// parent chain) and «Qwen3.8-27B投机解码实测：从14到159 tok/s的性能断点地图» (§2, §4:
+// 16-token pages from one pool; §5.3: bottom-right causal mask of a chain).
+//
+// Layout of the work.  A CTA owns (split s, KV head g, head part c, sequence
+// b).  The hpc query heads of the part (6 whenever 6 * N <= 144, i.e. trees
+// of up to 24 nodes) times the N draft nodes form NQ (multiple of 16, <= 144)
+// query columns, so each context page is read by one CTA only.  Per 128-token
+// tile:
+//   S^T[128 tok][NQ]      = K_tile[128 tok][256] . Q^T          (K-major A and B)
+//   O^T[256 dim][NQ]     += V_tile^T[256][128 tok] . P^T[128 tok][NQ]
+//                           (two M = 128 halves of the dims; MN-major A and B)
+// In tensor memory: S^T in columns [0, NQ), O^T in [NQ, 3 NQ) (dims 0-127, then
+// 128-255; one dim per lane).  P^T is the bf16 tile the softmax writes: 64-column
+// atoms with the 128-byte swizzle, and for NQ = 144 a 16-column tail with the
+// 32-byte swizzle.
+//
+// Rings.  K arrives in 16 KB slots, each one 64-dim block of a tile (one 2 KB
+// TMA box per page), and is released block by block as QK consumes it; V
+// arrives in 8 KB slots, one page each (one TMA box), released page by page as
+// PV consumes it (a page is one 16-token K-step of the PV product).  So while
+// the softmax works on tile i, the next tile's K blocks and this tile's
+// remaining V pages are already in flight, in whatever room the rings have.
+//
+// Warp roles (224 threads): warp 0 streams K, warp 6 streams V; warp 1
+// allocates tensor memory and one lane issues every tcgen05.mma, taking the
+// next QK block or the next PV page, whichever has its inputs; warps 2-5 (one
+// per tensor-memory lane quarter: thread = token row) run the online softmax
+// (running per-column maxima raised, with O and l rescaled, only when a score
+// exceeds them by more than 2^8) and write P^T, then in the epilogue (thread =
+// one dim of every query column) normalise and store the output rows.  Every
+// mbarrier wait is bounded; on expiry the kernel reports SD_DEV_TIMEOUT and
+// winds down.
+#pragma once
+
+#include <cstddef>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace sdv {
+namespace {
+
+constexpr int kT = kTileTokens;        // tokens per tile
+constexpr int kRingThreads = 224;
+constexpr int kRWarpK = 0, kRWarpMma = 1, kRWarpV = 6;
+constexpr int kKBlkB = kT * 128;       // K slot: one 64-dim block of a tile, 16 groups of 8 rows x 128 B
+constexpr int kPAtomB = kT * 128;      // one 64-column atom of P^T (128 token rows x 128 B)
+constexpr int kPTailB = kT * 32;       // the 16-column tail of P^T (128 token rows x 32 B)
+constexpr int kSmemMax = 232448;       // 227 KB of dynamic shared memory per CTA
+constexpr int kMaxStage = kRingMaxNQ + 2 * kMaxNodes;   // staging rows: Q^T + the draft block's K and V
+constexpr int kMaxBars = 44;
+constexpr float kThresh = 8.0f;        // base-2 growth of a maximum tolerated without rescaling
+constexpr float kNoMax = -1.0e30f;     // the running maximum before any visible score
+
+// Per-column state and barriers (COLS = query columns padded to 32).
+template <int COLS>
+struct RSmall {
+  float m[COLS];          // running maximum of each query column (base-2 score units)
+  float alpha[COLS];      // rescale factor of the current tile; 1/l of each column in the epilogue
+  int outrow[COLS];       // output row (node row * 24 + head) of each query column (-1: padding)
+  int lo_col[COLS];       // sliding window: oldest context position each query column sees
+  float red[4][COLS];     // per softmax warp: column maxima of a tile; column sums in the epilogue
+  uint64_t bar[kMaxBars];
+  unsigned long long anc[kMaxNodes];   // bit r of anc[n]: draft node r is node n or one of its ancestors
+  int par[kMaxNodes];
+  int depth[kMaxNodes];
+  int flag[2][4];
+  uint32_t tmem;
+  int abort;
+};
+
+template <int NQ>
+struct Ring {
+  static constexpr int NG = (NQ + 31) / 32;               // 32-column groups
+  static constexpr int kCols = NG * 32;
+  static constexpr bool kTail = NQ > 128;                  // columns 128.. in the 32-byte-swizzle tail
+  static constexpr int NQA = kTail ? 128 : NQ;             // columns in 64-column atoms
+  static constexpr int kPA = (NQA + 63) / 64;
+  static constexpr int kQB = NQ * 512;                     // Q^T: 4 blocks of NQ rows x 128 B
+  static constexpr int kPB = kPA * kPAtomB + (kTail ? kPTailB : 0);
+  static constexpr int kFixed = kQB + kPB + (int)sizeof(RSmall<kCols>);
+  static constexpr int kBudget = kSmemMax - kFixed;
+  static constexpr int RK = kBudget / 2 / kKBlkB < 4 ? 4 : (kBudget / 2 / kKBlkB > 8 ? 8 : kBudget / 2 / kKBlkB);
+  static constexpr int RV0 = (kBudget - RK * kKBlkB) / kPageB;
+  static constexpr int RV = RV0 > 16 ? 16 : RV0;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 5;
+  static constexpr size_t kSmem = (size_t)kQB + (size_t)RK * kKBlkB + (size_t)RV * kPageB + kPB + sizeof(RSmall<kCols>);
+  static_assert(RV >= 4 && RK >= 4, "the draft tile needs four K blocks and four V pages");
+  static_assert(kNumBars <= kMaxBars, "barrier array too small");
+  static_assert(kSmem <= (size_t)kSmemMax, "shared memory over 227 KB");
+  static_assert(kPB >= kMaxStage * 16, "the staging table lives in the P^T region");
+  static_assert(3 * NQ <= 512, "tensor memory holds S^T and both halves of O^T");
+};
+
+// WIN: compiled with the sliding-window paths (band masks, depths).
+template <int NQ, bool WIN>
+__global__ void __launch_bounds__(kRingThreads, 1)
+attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vp,
+                 const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
+  using R = Ring<NQ>;
+  constexpr int NG = R::NG, RK = R::RK, RV = R::RV, NQA = R::NQA, NPA = R::kPA;
+  constexpr bool TAIL = R::kTail;
+  constexpr uint32_t kColS = 0, kColO = NQ;   // tensor-memory columns: S^T, then O^T (two halves of NQ)
+  // Barriers: K slot full / empty, V slot full / empty, then the tile-level ones.
+  constexpr int B_KF = 0, B_KE = RK, B_VF = 2 * RK, B_VE = 2 * RK + RV;
+  constexpr int S_FULL = 2 * RK + 2 * RV, S_FREE = S_FULL + 1, P_FULL = S_FULL + 2, O_DONE = S_FULL + 3,
+                GROUP = S_FULL + 4;
+  // No static shared memory: the dynamic window starts on a 1024-byte boundary
+  // (the 128-byte swizzle atoms need it).
+  extern __shared__ __align__(1024) uint8_t dyn_smem[];
+  uint8_t* sQ = dyn_smem;
+  uint8_t* sK = sQ + R::kQB;
+  uint8_t* sV = sK + RK * kKBlkB;
+  uint8_t* sP = sV + RV * kPageB;
+  uint8_t* sPt = sP + NPA * kPAtomB;
+  using Sm = RSmall<R::kCols>;
+  Sm* sm = reinterpret_cast<Sm*>(sP + R::kPB);
+  // The staging table of the prologue (row source, destination, block stride)
+  // borrows the P^T region, which the softmax first writes after it.
+  const __nv_bfloat16** rsrc = reinterpret_cast<const __nv_bfloat16**>(sP);
+  uint32_t* rdst = reinterpret_cast<uint32_t*>(sP + 8 * kMaxStage);
+  uint32_t* rblk = rdst + kMaxStage;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool producer = warp == kRWarpK || warp == kRWarpV;
+  const int bid = blockIdx.x;
+  const int c = bid % hparts;
+  const int g = (bid / hparts) % kHkv;
+  const int s = bid / (hparts * kHkv);
+  const int b = blockIdx.y;
+  const int q0 = bd.q_indptr[b];
+  const int n_nodes = bd.q_indptr[b + 1] - q0;
+  const int rows = hpc * n_nodes;
+  if (c * hpc >= kGroup) return;
+  // Launched as a programmatic dependent of the previous kernel in the stream.
+  // By default every thread waits for that kernel before touching global
+  // memory.  With ctx_stable (the caller guarantees that kernel writes neither
+  // the context lengths, the page table nor the context pages) a context CTA's
+  // producers read those and issue their first tile's loads first, then wait;
+  // its compute warps wait before they read Q or the parents, so the outputs
+  // and the workspace are written only after the wait.  The draft CTA always
+  // waits here.  Then the merge kernel's blocks may be scheduled (they wait for
+  // this grid to finish before reading).
+  const bool early = p.ctx_stable != 0 && s != 0;
+  if (smem_u32(dyn_smem) & 1023u) {  // not expected; refuse rather than mis-swizzle
+    if (threadIdx.x == 0) report_dep(p.dev_status, SD_DEV_TIMEOUT);
+    return;
+  }
+  // The draft CTA (split 0) runs to the end in every case: it takes its tensor
+  // memory before the wait (no global memory involved).
+  if (s == 0 && warp == kRWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (producer && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kRWarpV ? &tm_vp : &tm_kb))
+                 : "memory");
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Split 0 attends to the draft block alone; split s >= 1 to context tokens
+  // [base + (s - 1) * chunk, base + s * chunk).  The producers fetch their first
+  // tile's page ids beside the context length (any entry of the row is in bounds).
+  const bool has_draft = (s == 0);
+  const int W = WIN ? p.window : 0;
+  int page0 = -1;
+  if (producer && lane < 8 && !has_draft && W <= 0) {
+    const long long idx = (((long long)(s - 1) * p.chunk) >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
+  int L = p.ctx_lens[b];
+  if (L < 0 || L > p.max_pages * kPage) {
+    if (s == 0 && c == 0 && g == 0 && tid == 0) report(p.dev_status, SD_DEV_BAD_CTX);
+    L = L < 0 ? 0 : p.max_pages * kPage;
+  }
+  const int base = window_base(L, W, kT);
+  const int nsplit = active_splits(L, W, kT, p.chunk);
+  if (s >= nsplit) return;
+  const int ctx_begin = has_draft ? 0 : base + (s - 1) * p.chunk;
+  if (W > 0 && producer && lane < 8 && !has_draft) {
+    const long long idx = (ctx_begin >> 4) + lane;
+    if (idx < p.max_pages) page0 = p.page_table[(size_t)b * p.max_pages + idx];
+  }
+  const int ctx_end = has_draft ? 0 : min(L, ctx_begin + p.chunk);
+  const int n_tiles = has_draft ? 1 : (ctx_end - ctx_begin + kT - 1) / kT;
+  const int head0 = g * kGroup + c * hpc;
+  // valid token rows of tile i (the draft tile: the block's nodes)
+  auto tile_valid = [&](int i) { return has_draft ? n_nodes : min(kT, ctx_end - (ctx_begin + i * kT)); };
+
+  // ---------------------------------------------------------------- prologue
+  if (tid == 0) {
+    for (int i = 0; i < R::kNumBars; ++i) {
+      const uint32_t cnt = (i == S_FREE || i == P_FULL || i == GROUP) ? 4u : 1u;
+      mbar_init(smem_u32(&sm->bar[i]), cnt);
+    }
+    sm->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int q = tid; q < R::kCols; q += kRingThreads) {
+    // Running maxima start finite and far below any score: a column that has
+    // seen no visible key yet (possible with a window) then gives masked scores
+    // exp2(-inf - m) = 0, not NaN, and its first visible score takes the
+    // rescaling path like any score more than 2^8 above the maximum.
+    sm->m[q] = q < NQ ? kNoMax : 0.f;
+    sm->alpha[q] = 1.f;
+    sm->outrow[q] = q < rows ? (q0 + q / hpc) * kHq + head0 + q % hpc : -1;
+  }
+  // one load each; the walks below are in shared memory (every CTA needs the depths with a window)
+  // (an early context CTA's compute warps load them after their wait)
+  if ((has_draft || (W > 0 && !early)) && tid < n_nodes) sm->par[tid] = p.parents[q0 + tid];
+  __syncthreads();  // mbarriers and per-column arrays ready
+  const uint32_t bars = smem_u32(&sm->bar[0]);
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+
+  // Staging of the operands that do not come by TMA, by `nthr` threads (index
+  // t): Q^T (K-major, block-major; column q = node * hpc + head-in-part, zeros
+  // past `rows`) and, in the draft CTA, the draft block: K rows into the four
+  // K slots (slot = 64-dim block; node t = token row t) and V rows into the
+  // first V slots (page layout).  A row table (source, destination, block
+  // stride) is built first, then one pass of 16-byte copies with up to 16
+  // loads in flight per thread; the last round repeats the final chunk instead
+  // of branching, so the unrolled copies stay independent.
+  auto stage_operands = [&](const int t, const int nthr, const bool all_warps) {
+    const float inv_hpc = 1.0f / (float)hpc;
+    const int n_stage = NQ + (has_draft ? 2 * n_nodes : 0);
+    for (int r = t; r < n_stage; r += nthr) {
+      const __nv_bfloat16* src;
+      uint32_t dst, blk;
+      if (r < NQ) {
+        const int node = __float2int_rz(((float)r + 0.5f) * inv_hpc);   // r / hpc, exact for r < 2^20
+        src = r < rows ? p.q + ((size_t)(q0 + node) * kHq + head0 + r - node * hpc) * kDim : nullptr;
+        dst = (uint32_t)(sQ - dyn_smem) + r * 128;
+        blk = NQ * 128;
+      } else {
+        const bool is_v = r >= NQ + n_nodes;
+        const int tok = r - NQ - (is_v ? n_nodes : 0);
+        src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + tok) * kHkv + g) * kDim;
+        if (is_v) {
+          dst = (uint32_t)(sV - dyn_smem) + (tok >> 3) * kGroupB + (tok & 7) * 128;
+          blk = 1024;
+        } else {
+          dst = (uint32_t)(sK - dyn_smem) + (tok >> 3) * 1024 + (tok & 7) * 128;
+          blk = kKBlkB;
+        }
+      }
+      rsrc[r] = src;
+      rdst[r] = dst;
+      rblk[r] = blk;
+    }
+    if (all_warps) __syncthreads();
+    else asm volatile("bar.sync 3, 160;" ::: "memory");   // the five compute warps
+    constexpr int U = 16;
+    const int tasks = n_stage * 32;
+    for (int t0 = t; t0 - t < tasks; t0 += nthr * U) {
+      uint4 v[U];
+      uint32_t d[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int task = min(t0 + u * nthr, tasks - 1);
+        const int r = task >> 5, cc = task & 31;
+        const __nv_bfloat16* src = rsrc[r];
+        const uint32_t off = rdst[r];
+        v[u] = src != nullptr ? __ldg(reinterpret_cast<const uint4*>(src) + cc) : make_uint4(0, 0, 0, 0);
+        d[u] = off + (cc >> 3) * rblk[r] + (((cc & 7) ^ ((off >> 7) & 7)) << 4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) *reinterpret_cast<uint4*>(dyn_smem + d[u]) = v[u];
+    }
+  };
+  if (has_draft) {
+    // The draft CTA has no TMA work: all warps stage its operands.  V rows from
+    // the block's end to the next 16-row boundary are zeroed (the draft tile's
+    // PV product stops there; P^T is 0 on them, but 0 times stale shared
+    // memory could be NaN).  K rows past the block are masked.
+    stage_operands(tid, kRingThreads, true);
+    const int v_end = (n_nodes + 15) & ~15;
+    for (int i = tid; i < (v_end - n_nodes) * 32; i += kRingThreads)
+      *reinterpret_cast<uint4*>(sV + kv_off(n_nodes + (i >> 5), i & 31)) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();   // plain stores above, read by the tensor core
+    __syncthreads();
+  }
+
+  if (producer) {
+    // ------------------------------------------------------------ producers (K: warp 0, V: warp 6)
+    const bool is_k = warp == kRWarpK;
+    const int n_ctx = has_draft ? 0 : n_tiles;
+    const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
+    int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
+    int slot = 0, fills = 0;
+    uint32_t ph = 0;
+    const int ring = is_k ? RK : RV;
+    bool ok = true;
+    for (int i = 0; i < n_ctx && ok; ++i) {
+      const int t0 = ctx_begin + i * kT;
+      const int valid = min(kT, ctx_end - t0);
+      int page = (lane < 8 && lane * kPage < valid) ? page_next : -1;
+      if (lane < 8 && i + 1 < n_ctx && lane * kPage < ctx_end - (t0 + kT))
+        page_next = p.page_table[(size_t)b * p.max_pages + (((t0 + kT) >> 4) + lane)];
+      bool bad = false;
+      if (lane < 8 && lane * kPage < valid && (page < 0 || page >= p.num_pool_pages)) {
+        if (is_k) report_dep(p.dev_status, SD_DEV_BAD_PAGE);
+        page = -1;
+        bad = true;
+      }
+      if (is_k) {
+        // K: four 64-dim blocks per tile, each a slot of eight 2 KB boxes.
+        // Pages past the context are not loaded (their rows are masked);
+        // pages with an id out of range are zeros.
+        const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page >= 0);
+        const uint32_t zero_mask = __ballot_sync(0xffffffffu, bad);
+        for (int kb = 0; kb < 4; ++kb) {
+          if (lane == 0) ok = mbar_wait(bar(B_KE + slot), ph ^ 1u, &sm->abort, p.dev_status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          uint8_t* dst = sK + slot * kKBlkB;
+          if (zero_mask != 0u) {
+            for (uint32_t zm = zero_mask; zm != 0u; zm &= zm - 1u) {
+              const int pi = __ffs(zm) - 1;
+              for (int e = lane; e < 2048 / 16; e += 32)
+                *reinterpret_cast<uint4*>(dst + pi * 2048 + e * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_KF + slot), (uint32_t)__popc(tma_mask) * 2048u);
+          __syncwarp();
+          if ((tma_mask >> lane) & 1u)
+            tma_load_kblk(smem_u32(dst + lane * 2048), &tm_kb, kb, (page * kHkv + g) * 2, bar(B_KF + slot));
+          ++fills;
+          if (++slot == ring) { slot = 0; ph ^= 1u; }
+        }
+      } else {
+        // V: the tile's pages up to the last valid token, one slot each.  A
+        // page goes by TMA when it is in range and all its 16 tokens are valid;
+        // otherwise plain loads, zero past the context (P is 0 there, but 0
+        // times stale data could be NaN).
+        const int npg = (valid + kPage - 1) / kPage;
+        for (int j = 0; j < npg; ++j) {
+          if (lane == 0) ok = mbar_wait(bar(B_VE + slot), ph ^ 1u, &sm->abort, p.dev_status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const int pg = __shfl_sync(0xffffffffu, page, j);
+          const bool full = pg >= 0 && (j + 1) * kPage <= valid;
+          uint8_t* dst = sV + slot * kPageB;
+          if (!full) {
+            stage_rows(dst, 0, kPage, [&](int r) -> const __nv_bfloat16* {
+              return (pg >= 0 && j * kPage + r < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + r) * kDim
+                                                        : nullptr;
+            }, lane, 32);
+            fence_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(bar(B_VF + slot), full ? (uint32_t)kPageB : 0u);
+            if (full) tma_load_page(smem_u32(dst), &tm_vp, (pg * kHkv + g) * 2, bar(B_VF + slot));
+          }
+          ++fills;
+          if (++slot == ring) { slot = 0; ph ^= 1u; }
+        }
+      }
+      // early context loads: the later slots free up only as the compute warps (which wait) progress
+      if (early && i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (__shfl_sync(0xffffffffu, *(volatile int*)&sm->abort, 0)) break;
+    }
+    // After an abort no copy may still be landing when the CTA ends: wait,
+    // bounded, for the last fill of every slot.
+    if (lane == 0 && *(volatile int*)&sm->abort) {
+      for (int j = 0; j < ring && j < fills; ++j) {
+        const uint32_t parity = j < slot ? ph : ph ^ 1u;   // the last fill of slot j
+        const long long t0 = clock64();
+        while (!mbar_test(bar((is_k ? B_KF : B_VF) + j), parity) && clock64() - t0 < kWaitCycles) {
+        }
+      }
+    }
+  } else {
+  // ---------------------------------------------------------------- compute warps (1-5)
+  // While the producers fetch the first tiles, these five warps stage Q^T and
+  // allocate tensor memory.
+  {
+    const int ct = tid - 32;
+    if (early) {
+      // tensor memory first (no global memory), then the wait for the previous kernel
+      if (warp == kRWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (W > 0)
+        for (int j = ct; j < n_nodes; j += 5 * 32) sm->par[j] = p.parents[q0 + j];
+    }
+    if (!has_draft) stage_operands(ct, 5 * 32, false);
+    if (W > 0) {
+      // oldest visible context position of each query column: L + depth(node) - W + 1
+      // (padding columns take the root's; an invalid parent chain stops the walk)
+      const float inv_hpc = 1.0f / (float)hpc;
+      for (int q = ct; q < R::kCols; q += 5 * 32) {
+        int d = 0;
+        if (q < rows) {
+          for (int u = __float2int_rz(((float)q + 0.5f) * inv_hpc); u > 0 && d < kMaxNodes; ++d) {
+            const int pu = sm->par[u];
+            if (pu < 0 || pu >= u) break;
+            u = pu;
+          }
+        }
+        sm->lo_col[q] = L + d - W + 1;
+      }
+    }
+    if (warp == kRWarpMma && !early && s != 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_fence_before();
+    asm volatile("bar.sync 1, 160;" ::: "memory");   // the five compute warps, all arrive unconditionally
+    tc_fence_after();
+  }
+  const uint32_t tmem = sm->tmem;
+  if (warp == kRWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = f16_idesc(128, NQ, 0, 0);
+      constexpr uint32_t kIdPV = f16_idesc(128, NQA, 1, 1);
+      constexpr uint32_t kIdPVt = f16_idesc(128, 16, 1, 1);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const uint32_t p_addr = smem_u32(sP), pt_addr = smem_u32(sPt);
+      int ks = 0, vs = 0;          // ring slots
+      uint32_t kph = 0, vph = 0;   // their fill parities
+      int qk_i = 0, qk_b = 0;      // QK: tile, next 64-dim block
+      int pv_i = 0, pv_j = 0;      // PV: tile, next page
+      int pv_pages = (tile_valid(0) + kPage - 1) / kPage;
+      long long idle_since = clock64();
+      while (pv_i < n_tiles) {
+        bool progressed = false;
+        // QK, one 64-dim block: the block's slot has landed, and for a tile's
+        // first block the softmax has read the previous S^T
+        if (qk_i < n_tiles) {
+          const bool s_ok = qk_b > 0 || qk_i == 0 || mbar_test(bar(S_FREE), (uint32_t)(qk_i - 1) & 1u);
+          const bool k_ok = has_draft || mbar_test(bar(B_KF + ks), kph);
+          if (s_ok && k_ok) {
+            tc_fence_after();
+            const uint32_t ka = k_addr + (uint32_t)ks * kKBlkB;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // A = K block, K-major: 8-row groups 1 KB apart, 32 bytes per 16-dim step;
+              // B = Q^T block qk_b, K-major: 8-row groups 1 KB apart
+              umma(tmem + kColS, sw128_desc(ka + k * 32, 16, 1024),
+                   sw128_desc(q_addr + (uint32_t)qk_b * NQ * 128 + k * 32, 16, 1024), kIdQK,
+                   (qk_b | k) != 0 ? 1u : 0u);
+            }
+            if (!has_draft) umma_commit(bar(B_KE + ks));
+            if (++ks == RK) { ks = 0; kph ^= 1u; }
+            if (++qk_b == 4) {
+              umma_commit(bar(S_FULL));
+              qk_b = 0;
+              ++qk_i;
+            }
+            progressed = true;
+          }
+        }
+        // PV, one page (16 tokens): P^T of the tile is written, the page has landed
+        if (pv_i < qk_i) {
+          const bool p_ok = pv_j > 0 || mbar_test(bar(P_FULL), (uint32_t)pv_i & 1u);
+          const bool v_ok = has_draft || mbar_test(bar(B_VF + vs), vph);
+          if (p_ok && v_ok) {
+            tc_fence_after();
+            const uint32_t va = v_addr + (uint32_t)vs * kPageB;
+            const uint32_t acc = (pv_i > 0 || pv_j > 0) ? 1u : 0u;
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+              // A = V^T, dims mb*128.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart;
+              // B = P^T rows 16 pv_j.., MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
+              const uint64_t a = sw128_desc(va + mb * 2048, 1024, kGroupB);
+              umma(tmem + kColO + mb * NQ, a, sw128_desc(p_addr + pv_j * 2048, kPAtomB, 1024), kIdPV, acc);
+              if (TAIL)   // columns 128-143: 32-byte rows, 8-token groups 256 B apart
+                umma(tmem + kColO + mb * NQ + 128, a, sw32_desc(pt_addr + pv_j * 512, kPTailB, 256), kIdPVt, acc);
+            }
+            if (!has_draft) umma_commit(bar(B_VE + vs));
+            if (++vs == RV) { vs = 0; vph ^= 1u; }
+            if (++pv_j == pv_pages) {
+              umma_commit(bar(O_DONE));
+              pv_j = 0;
+              ++pv_i;
+              if (pv_i < n_tiles) pv_pages = (tile_valid(pv_i) + kPage - 1) / kPage;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = clock64();
+        } else {
+          if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
+            sm->abort = 1;
+            report(p.dev_status, SD_DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(20);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int sw = warp - 2;                 // 0..3
+    const int quarter = warp & 3;            // tensor-memory lane quarter of this warp
+    const int row = quarter * 32 + lane;     // token row of S^T; dim (mod 128) of O^T in the epilogue
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + kColS;
+    int gphase = 0;
+    // Barrier of the four softmax warps on an mbarrier, so that it is bounded too.
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(GROUP));
+      return mbar_spin(bar(GROUP), (uint32_t)(gphase++ & 1), &sm->abort, p.dev_status);
+    };
+    auto load_cols = [&](const float* arr, int col, float (&w)[32]) {
+      const float4* src = reinterpret_cast<const float4*>(arr + col);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 t = src[k];
+        w[4 * k] = t.x; w[4 * k + 1] = t.y; w[4 * k + 2] = t.z; w[4 * k + 3] = t.w;
+      }
+    };
+    // Column sums of P from the bf16 tile this warp wrote (the same rounded
+    // weights the PV product multiplies V with).  Atoms: lane L sums columns
+    // 64a + 8(L%8) .. +7 over token rows 32 quarter + L/8 + 4k, k < 8.  Tail:
+    // columns 128 + 8(L%2) .. +7 over rows 32 quarter + L/2 + 16k, k < 2.  The
+    // lanes and the four warps are added in the epilogue.
+    float csum[NPA][8];
+    float csum_t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      csum_t[j] = 0.f;
+#pragma unroll
+      for (int a = 0; a < NPA; ++a) csum[a][j] = 0.f;
+    }
+    const int cs_chunk = lane & 7;
+    // Draft CTA: the tree masks.  Node `row` walks its root path (its ancestor
+    // set), then, after the group barrier, gathers its descendant set: bit n
+    // set when node n has `row` on its root path (itself included).
+    unsigned long long my_desc = 0ull;
+    bool masks_ok = true;
+    if (has_draft) {
+      if (row < n_nodes) {
+        unsigned long long a = 1ull << row;
+        int d = 0;
+        bool okp = row == 0 ? sm->par[0] == -1 : true;
+        for (int u = row; okp && u > 0; ++d) {
+          const int pu = sm->par[u];
+          okp = pu >= 0 && pu < u;
+          if (okp) a |= 1ull << pu;
+          u = pu;
+        }
+        if (!okp) { report(p.dev_status, SD_DEV_BAD_PARENTS); a = 1ull << row; d = 0; }
+        sm->anc[row] = a;
+        sm->depth[row] = d;
+      }
+      masks_ok = group_sync();
+      if (row < n_nodes) {
+        // with a window, a descendant n more than W - 1 levels below does not see `row`
+        const int dr = sm->depth[row];
+        for (int n = row; n < n_nodes; ++n)
+          if (W <= 0 || sm->depth[n] - dr < W) my_desc |= ((sm->anc[n] >> row) & 1ull) << n;
+      }
+    }
+    uint32_t pk[NQ / 2];   // this token row's bf16 P, column pairs
+    for (int i = 0; i < n_tiles && masks_ok; ++i) {
+      if (!mbar_spin(bar(S_FULL), (uint32_t)i & 1u, &sm->abort, p.dev_status)) break;
+      tc_fence_after();
+      const int t0 = ctx_begin + i * kT;
+      const int valid = tile_valid(i);
+      // Visibility of this thread's token row, one bit per column of each
+      // 32-column group: context rows before `valid` see every query column;
+      // in the draft tile, node `row` is seen by the columns of its
+      // descendants (itself included; padding columns see the root only).
+      uint32_t vis[NG];
+#pragma unroll
+      for (int gq = 0; gq < NG; ++gq) {
+        const int ncol = min(32, NQ - gq * 32);
+        vis[gq] = (!has_draft && row < valid) ? (ncol >= 32 ? 0xffffffffu : ((1u << ncol) - 1u)) : 0u;
+      }
+      if (!has_draft && W > 0 && t0 < L - W + 1 + kMaxNodes) {
+        // tiles inside the window's band: column q sees token t0 + row from lo_col[q] on
+        const int tpos = t0 + row;
+#pragma unroll
+        for (int gq = 0; gq < NG; ++gq) {
+          uint32_t bits = 0u;
+#pragma unroll 1
+          for (int e = 0; e < 32; ++e) bits |= (tpos >= sm->lo_col[gq * 32 + e] ? 1u : 0u) << e;
+          vis[gq] &= bits;
+        }
+      }
+      if (has_draft) {
+        unsigned long long d = my_desc;
+        while (d != 0ull) {
+          const int n = __ffsll((long long)d) - 1;
+          d &= d - 1ull;
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(n * hpc - gq * 32, hpc);
+        }
+        if (row == 0) {
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) vis[gq] |= bit_range(rows - gq * 32, NQ - rows);
+        }
+      }
+      // Scores of group g32 of this thread's token row (32 columns, 16 for a
+      // tail group), base 2, masked to -inf.
+      auto load_scores = [&](int g32, float (&v)[32]) {
+        float a[16], cc[16];
+        const bool second = g32 * 32 + 16 < NQ;
+        tmem_ld16(s_addr + g32 * 32, a);
+        if (second) tmem_ld16(s_addr + g32 * 32 + 16, cc);
+        tmem_wait_ld();
+        const uint32_t vm = vis_of(vis, g32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float raw = e < 16 ? a[e] : (second ? cc[e - 16] : 0.f);
+          v[e] = ((vm >> e) & 1u) ? raw * kScaleLog2 : -INFINITY;
+        }
+      };
+      // P = exp2(s - m) of group g32 into the packed row; returns the largest s - m.
+      auto make_p = [&](int g32, const float (&v)[32]) -> float {
+        float mm[32];
+        load_cols(sm->m, g32 * 32, mm);
+        float dm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          if (g32 * 32 + e < NQ) {
+            const float d0 = v[e] - mm[e], d1 = v[e + 1] - mm[e + 1];
+            dm = fmaxf(dm, fmaxf(d0, d1));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(fast_exp2(d0), fast_exp2(d1));
+            pk[(g32 * 32 + e) / 2] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+        return dm;
+      };
+      // Fast pass (every tile after the first): P with the running maxima,
+      // and whether any score exceeds its column's maximum by more than 2^8.
+      bool slow = true;
+      if (i > 0) {
+        float dmax = -INFINITY;
+#pragma unroll
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32];
+          load_scores(g32, v);
+          dmax = fmaxf(dmax, make_p(g32, v));
+        }
+        if (lane == 0) sm->flag[i & 1][sw] = 0;
+        __syncwarp();
+        if (__any_sync(0xffffffffu, dmax > kThresh) && lane == 0) sm->flag[i & 1][sw] = 1;
+        if (!group_sync()) break;
+        slow = (sm->flag[i & 1][0] | sm->flag[i & 1][1] | sm->flag[i & 1][2] | sm->flag[i & 1][3]) != 0;
+      }
+      if (slow) {
+        // exact column maxima of this tile, new running maxima and rescale factors
+#pragma unroll 1
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32];
+          load_scores(g32, v);
+          sm->red[sw][g32 * 32 + lane] = transpose_max32(v, lane);
+        }
+        if (!group_sync()) break;
+        for (int q = sw * 32 + lane; q < NQ; q += 128) {
+          const float mt = fmaxf(fmaxf(sm->red[0][q], sm->red[1][q]), fmaxf(sm->red[2][q], sm->red[3][q]));
+          const float mo = sm->m[q];
+          const float mn = fmaxf(mo, mt);
+          sm->alpha[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+          sm->m[q] = mn;
+        }
+        if (!group_sync()) break;
+#pragma unroll
+        for (int g32 = 0; g32 < NG; ++g32) {
+          float v[32];
+          load_scores(g32, v);
+          make_p(g32, v);
+        }
+      }
+      // S^T is read: the next tile's QK may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_FREE));
+      // P^T and O belong to the previous tile's PV until it has finished
+      if (i > 0 && !mbar_spin(bar(O_DONE), (uint32_t)(i - 1) & 1u, &sm->abort, p.dev_status)) break;
+      tc_fence_after();
+      if (slow && i > 0) {
+        // rescale what O^T and the column sums hold to the new maxima: this
+        // thread's dim (both halves) across every query column
+#pragma unroll
+        for (int a = 0; a < NPA; ++a) {
+          const float4 f0 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[0];
+          const float4 f1 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[1];
+          csum[a][0] *= f0.x; csum[a][1] *= f0.y; csum[a][2] *= f0.z; csum[a][3] *= f0.w;
+          csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
+        }
+        if (TAIL) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) csum_t[j] *= sm->alpha[128 + 8 * (lane & 1) + j];
+        }
+#pragma unroll 1
+        for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll 1
+          for (int q = 0; q < NQ; q += 16) {
+            float v[16];
+            const uint32_t ad = tmem + lane_addr + kColO + mb * NQ + q;
+            tmem_ld16(ad, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= sm->alpha[q + e];
+            tmem_st16(ad, v);
+          }
+        }
+        tmem_wait_st();
+      }
+      // P^T row of this token: 64-column atoms, then the tail
+#pragma unroll
+      for (int ch = 0; ch < NQ / 8; ++ch) {
+        const uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        if (ch < NQA / 8) {
+          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kPAtomB + p_off(row, ch & 7)) = w;
+        } else {
+          const int tc = ch - NQA / 8;   // 0 or 1
+          *reinterpret_cast<uint4*>(sPt + row * 32 + ((tc ^ ((row >> 2) & 1)) << 4)) = w;
+        }
+      }
+      tc_fence_before();
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+      // Column sums of this tile's P from the rows this warp just wrote, while
+      // the PV product runs (the next tile overwrites P^T only after it ends).
+#pragma unroll
+      for (int a = 0; a < NPA; ++a) {
+        if (a * 64 + cs_chunk * 8 < NQA) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = quarter * 32 + (lane >> 3) + 4 * k;
+            const uint4 pv = *reinterpret_cast<const uint4*>(sP + a * kPAtomB + p_off(r, cs_chunk));
+            const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
+              csum[a][2 * e] += f.x;
+              csum[a][2 * e + 1] += f.y;
+            }
+          }
+        }
+      }
+      if (TAIL) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int r = quarter * 32 + (lane >> 1) + 16 * k;
+          const uint4 pv = *reinterpret_cast<const uint4*>(sPt + r * 32 + (((lane & 1) ^ ((r >> 2) & 1)) << 4));
+          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
+            csum_t[2 * e] += f.x;
+            csum_t[2 * e + 1] += f.y;
+          }
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // Column sums l: the lanes with the same columns, then the four warps
+    // (through red[], free now).  Thread `row` then holds dim `row` (and
+    // 128 + row) of every query column in its tensor-memory lane; it scales by
+    // 1/l and adjacent lanes pair their dims, so that each 4-byte store writes
+    // two dims of one output row (64 bytes per row per store instruction).
+    bool ok_epi = !*(volatile int*)&sm->abort;
+    if (ok_epi) {
+#pragma unroll
+      for (int a = 0; a < NPA; ++a)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 8);
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 16);
+        }
+      if (TAIL) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 2);
+          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 4);
+          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 8);
+          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 16);
+        }
+      }
+      // red[] may still be read by another warp's last max reduction: barrier first
+      ok_epi = group_sync();
+      if (ok_epi) {
+        if (lane < 8) {
+#pragma unroll
+          for (int a = 0; a < NPA; ++a) {
+            if (a * 64 + lane * 8 < NQA) {
+              float4* dst = reinterpret_cast<float4*>(&sm->red[sw][a * 64 + lane * 8]);
+              dst[0] = make_float4(csum[a][0], csum[a][1], csum[a][2], csum[a][3]);
+              dst[1] = make_float4(csum[a][4], csum[a][5], csum[a][6], csum[a][7]);
+            }
+          }
+        }
+        if (TAIL && lane < 2) {
+          float4* dst = reinterpret_cast<float4*>(&sm->red[sw][128 + lane * 8]);
+          dst[0] = make_float4(csum_t[0], csum_t[1], csum_t[2], csum_t[3]);
+          dst[1] = make_float4(csum_t[4], csum_t[5], csum_t[6], csum_t[7]);
+        }
+        ok_epi = group_sync();
+      }
+    }
+    if (ok_epi && mbar_spin(bar(O_DONE), (uint32_t)(n_tiles - 1) & 1u, &sm->abort, p.dev_status)) {
+      tc_fence_after();
+      const bool direct = nsplit == 1;
+      const size_t part0 = (size_t)s * bd.total_nodes * kHq;
+      // 1/l and the log-sum-exp of each query column (base 2 for the merge); a
+      // column with no visible key in this split gives 0 and -inf
+      for (int q = sw * 32 + lane; q < NQ; q += 128) {
+        const float lq = sm->red[0][q] + sm->red[1][q] + sm->red[2][q] + sm->red[3][q];
+        sm->alpha[q] = lq > 0.f ? 1.0f / lq : 0.f;
+        if (q < rows) {
+          const float lse2 = sm->m[q] + fast_log2(lq);
+          if (direct) {
+            if (p.lse != nullptr) p.lse[sm->outrow[q]] = lse2 * kLn2;
+          } else {
+            p.lse_part[part0 + sm->outrow[q]] = lse2;
+          }
+        }
+      }
+      if (group_sync()) {
+        uint8_t* gbase = reinterpret_cast<uint8_t*>(direct ? p.out : p.o_part + part0 * kDim);
+        const bool odd = (lane & 1) != 0;
+        const int dpair = (row & ~1) * 2;   // byte offset of this lane pair's two dims
+        const int nq16 = (rows + 15) / 16;
+#pragma unroll 1
+        for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll 1
+          for (int q16 = 0; q16 < nq16; ++q16) {
+            const int qb = q16 * 16;
+            float v[16];
+            tmem_ld16(tmem + lane_addr + kColO + mb * NQ + qb, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float ev = v[2 * k] * sm->alpha[qb + 2 * k];
+              const float od = v[2 * k + 1] * sm->alpha[qb + 2 * k + 1];
+              // even lanes keep the even column and take the odd lane's dim of it; odd lanes the reverse
+              const float recv = __shfl_xor_sync(0xffffffffu, odd ? ev : od, 1);
+              const float lo = odd ? recv : ev, hi = odd ? od : recv;
+              const int q = qb + 2 * k + (odd ? 1 : 0);
+              if (q < rows) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+                *reinterpret_cast<uint32_t*>(gbase + ((size_t)sm->outrow[q] << 9) + mb * 256 + dpair) =
+                    *reinterpret_cast<const uint32_t*>(&h);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  }  // compute warps
+  __syncthreads();
+  if (warp == kRWarpMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm->tmem));
+  }
+}
+
+}  // namespace
+}  // namespace sdv

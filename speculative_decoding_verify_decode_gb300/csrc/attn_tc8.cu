@@ -1,7 +1,7 @@
 // Host side of the split-KV verify attention on e4m3 (quantised) caches: the
-// tensor map of the K codes (V pages move as plain bulk copies); the launch
-// plan and the merge are those of the bf16 caches.  The kernel itself is in
-// attn_tc_kernel.cuh.
+// tensor map of the K codes (V pages move as plain bulk copies), the
+// query-column plan of this kernel, and the launch followed by the merge.  The
+// kernel itself is in attn_tc_kernel.cuh.
 #include "attn_tc_kernel.cuh"
 
 namespace sdv {
@@ -24,6 +24,24 @@ bool code_map(CUtensorMap* map, const void* cache, int pool_pages) {
 }
 
 }  // namespace
+
+size_t tc_smem_bytes(int nq) {
+  // the P^T tile always spans two 64-column atoms: the PV product takes its 128 rows as M
+  return (size_t)nq * 512 + 2 * (size_t)kTileB + 2 * (size_t)kAtomB + sizeof(Small);
+}
+
+TcPlan tc_plan(int max_nodes) {
+  TcPlan pl;
+  const int opts[4] = {6, 3, 2, 1};
+  pl.hpc = 1;
+  for (int h : opts) {
+    if (h * max_nodes <= kTcMaxNQ) { pl.hpc = h; break; }
+  }
+  pl.hparts = (kGroup + pl.hpc - 1) / pl.hpc;
+  pl.nq = (pl.hpc * max_nodes + 15) / 16 * 16;
+  if (pl.nq < 32) pl.nq = 32;
+  return pl;
+}
 
 cudaError_t launch_attn_tc8(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   CUtensorMap mk, unused;   // V pages move as plain bulk copies

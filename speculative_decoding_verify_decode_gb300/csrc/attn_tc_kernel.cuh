@@ -69,13 +69,12 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace sdv {
 namespace {
 
 constexpr int kT = kTileTokens;         // tokens per tile
-constexpr int kGroupB = 4096;           // 8 token rows x 4 dim blocks x 128 B
-constexpr int kPageB = 2 * kGroupB;     // one page of one KV head: 16 rows x 256 dims
 constexpr int kTileB = kT / 8 * kGroupB;   // 64 KB
 constexpr int kAtomB = kT * 128;        // one 64-column atom of the P^T tile: 16 KB
 constexpr int kThreads = 224;
@@ -88,7 +87,6 @@ constexpr int kHalfB = kTileB / 2;      // quantised cache: f16 half tile (128 t
 constexpr int kSlotB = kTileB / 4;      // quantised cache: e4m3 half tile (staging slot)
 constexpr float kThresh = 8.0f;         // base-2 growth of the max tolerated without rescaling
 constexpr float kNoMax = -1.0e30f;      // the running maximum before any visible score
-constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 
 // The V tile moves in two 64-token halves (pages 0-3 and 4-7, each 32 KB
 // contiguous), so that the first half of the next tile loads while the PV
@@ -130,178 +128,6 @@ static_assert(offsetof(Small, bar) % 8 == 0, "mbarriers must be 8-byte aligned")
 static_assert(kTcMaxNQ * 512 + 2 * kTileB + 2 * kAtomB + sizeof(Small) <= 232448,
               "the widest tile configuration must fit in 227 KB of shared memory");
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// ------------------------------------------------------------ mbarrier / TMA
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-// Test a phase; the waiting thread is suspended in hardware (up to about
-// 10 ms, or until the phase completes) instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(10000000u)
-      : "memory");
-  return ok != 0;
-}
-// Non-blocking test of a phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false (and the CTA's abort flag set) if the phase never completes.
-// Status bits from a thread that may not have waited for the previous kernel
-// yet (context loads issued before the wait): wait first, so that the bit
-// cannot be lost to a predecessor that resets the status word.  A no-op wait
-// once the predecessor has finished.
-__device__ __forceinline__ void report_dep(int* status, int bits) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  report(status, bits);
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Small* sm, int* status) {
-  const long long t0 = clock64();
-  while (!mbar_try(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
-      sm->abort = 1;
-      report_dep(status, SD_DEV_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-// Bounded spin on a phase (no suspension): the softmax warps have nothing
-// else to do while they wait, and a spin sees the phase flip soonest.
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, Small* sm, int* status) {
-  const long long t0 = clock64();
-  while (!mbar_test(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles || *(volatile int*)&sm->abort) {
-      sm->abort = 1;
-      report_dep(status, SD_DEV_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// One page of one KV head (8 KB) into shared memory: the 4-D box of the
-// cache map at outer coordinate w, x = y = z = 0.
-__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
-      : "memory");
-}
-
-// ------------------------------------------------------------ tcgen05
-
-// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
-// stride byte offsets (16-byte units), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor of kind::f16: bf16 x bf16 (or f16 x f16) -> f32, M x N, operand majors.
-__host__ __device__ constexpr uint32_t f16_idesc(int m, int n, int a_mn, int b_mn, bool bf16 = true) {
-  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-
-// Byte offset of 16-byte chunk c (0..31) of token row r in a group-major
-// K/V tile: 8-row group r/8 (4 KB), 64-dim block c/8 (1 KB), row r%8,
-// swizzled chunk (c%8) ^ (r%8).  A page's 16 rows are 8 contiguous KB.
-__device__ __forceinline__ uint32_t kv_off(int r, int c) {
-  return (uint32_t)((r >> 3) * kGroupB + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-// Byte offset of 16-byte chunk cc (0..7) of token row r in the P^T tile
-// (MN-major: 64-column atoms of 128 rows x 128 B, 128-byte swizzle).
-__device__ __forceinline__ uint32_t p_off(int r, int cc) {
-  return (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
-}
-
-// Copy `nrows` rows of 256 bf16 into rows r0.. of a group-major K/V tile
-// (row r's source is src_of(r), or zeros when that is null).  `nthreads`
-// threads starting at `t` share the work; each keeps 8 independent 16-byte
-// loads in flight.
-template <typename SrcFn>
-__device__ __forceinline__ void stage_rows(uint8_t* base, int r0, int nrows, SrcFn src_of, int t, int nthreads) {
-  constexpr int U = 8;
-  const int tasks = nrows * 32;
-  for (int t0 = t; t0 < tasks; t0 += nthreads * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int task = t0 + u * nthreads;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (task < tasks) {
-        const __nv_bfloat16* src = src_of(task >> 5);
-        if (src != nullptr) v[u] = __ldg(reinterpret_cast<const uint4*>(src) + (task & 31));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int task = t0 + u * nthreads;
-      if (task < tasks) *reinterpret_cast<uint4*>(base + kv_off(r0 + (task >> 5), task & 31)) = v[u];
-    }
-  }
-}
-
 // ------------------------------------------------------------ quantised cache
 
 // Eight bf16 (one 16-byte chunk) as eight f16, rounded to nearest.
@@ -334,40 +160,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
-// Bits [start, start + len) of a 32-bit word (clipped to the word).
-__device__ __forceinline__ uint32_t bit_range(int start, int len) {
-  const int a = max(start, 0), e = min(start + len, 32);
-  if (e <= a) return 0u;
-  const uint32_t upto = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
-  return upto & ~((1u << a) - 1u);
-}
-
-// Element g of a small per-thread array, by a select chain rather than a
-// dynamically indexed (local-memory) access.
-template <int N>
-__device__ __forceinline__ uint32_t vis_of(const uint32_t (&a)[N], int g) {
-  uint32_t r = a[0];
-#pragma unroll
-  for (int k = 1; k < N; ++k) r = (g == k) ? a[k] : r;
-  return r;
-}
-
-// Reduce 32 values per lane across the warp so that lane L ends with the
-// maximum over all lanes of value L (transpose-reduce, 31 shuffles).
-__device__ __forceinline__ float transpose_max32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool up = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = up ? v[i] : v[i + half];
-      const float keep = up ? v[i + half] : v[i];
-      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
-    }
-  }
-  return v[0];
-}
-
 // WIN: compiled with the sliding-window paths (band masks, depths); the
 // instances without them serve full attention.
 // KV8: the quantised-cache instance (e4m3 pages, f16 operands, converter warps).
@@ -669,8 +461,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           const uint32_t slot_full = bar(is_k ? K8_FULL0 + h : V8_FULL0 + h);
           const uint32_t buf_empty = bar(is_k ? K_EMPTY : V_EMPTY0);
           if (lane == 0)
-            ok = mbar_wait(slot_full, (uint32_t)(i & 1), sm, p.dev_status) &&
-                 mbar_wait(buf_empty, (uint32_t)(uses & 1) ^ 1u, sm, p.dev_status);
+            ok = mbar_wait(slot_full, (uint32_t)(i & 1), &sm->abort, p.dev_status) &&
+                 mbar_wait(buf_empty, (uint32_t)(uses & 1) ^ 1u, &sm->abort, p.dev_status);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           const uint32_t src_base = smem_u32((is_k ? sK8 : sV8) + h * kSlotB) + src0;
@@ -755,7 +547,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       for (int part = 0; part < nparts && ok; ++part) {
         const uint32_t full = bar(is_k ? K_FULL : V_FULL0 + part), empty = bar(is_k ? K_EMPTY : V_EMPTY0 + part);
         const uint32_t part_mask = ((1u << ppp) - 1u) << (part * ppp);
-        if (lane == 0) ok = mbar_wait(empty, parity, sm, p.dev_status);
+        if (lane == 0) ok = mbar_wait(empty, parity, &sm->abort, p.dev_status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // pages that are partial, missing or out of range: plain copies, zero past the context
@@ -955,7 +747,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     auto group_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(GROUP));
-      return mbar_spin(bar(GROUP), (uint32_t)(gphase++ & 1), sm, p.dev_status);
+      return mbar_spin(bar(GROUP), (uint32_t)(gphase++ & 1), &sm->abort, p.dev_status);
     };
     auto load_cols = [&](const float* arr, int col, float (&w)[32]) {
       const float4* src = reinterpret_cast<const float4*>(arr + col);
@@ -1006,7 +798,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     for (int i = 0; i < n_tiles && masks_ok; ++i) {
       const int sb = i & 1;
-      if (!mbar_spin(bar(S_FULL0 + sb), (i >> 1) & 1, sm, p.dev_status)) break;
+      if (!mbar_spin(bar(S_FULL0 + sb), (i >> 1) & 1, &sm->abort, p.dev_status)) break;
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + kColS0 + sb * NQ;
       const bool draft_tile = has_draft;
@@ -1139,7 +931,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (i > 0) {
           // O holds earlier tiles: wait for the last PV, then rescale the rows
           // (query columns) of this warp's lane quarter, 32 dims at a time
-          if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+          if (!mbar_spin(bar(O_DONE), (i - 1) & 1, &sm->abort, p.dev_status)) break;
           pv_waited = true;
           tc_fence_after();
           if (quarter * 32 < NQ) {   // warp-uniform: the quarter holds query columns
@@ -1162,7 +954,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
       // Pass 2: P = exp2(s - m) as the bf16 P^T row of this token.
       if (i > 0 && !pv_waited) {
-        if (!mbar_spin(bar(O_DONE), (i - 1) & 1, sm, p.dev_status)) break;
+        if (!mbar_spin(bar(O_DONE), (i - 1) & 1, &sm->abort, p.dev_status)) break;
       }
       auto write_p = [&](int g32, const float (&v)[32]) {
         float mm[32];
@@ -1250,7 +1042,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
     }
     if (!*(volatile int*)&sm->abort && group_sync() &&
-        mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, sm, p.dev_status)) {
+        mbar_spin(bar(O_DONE), (n_tiles - 1) & 1, &sm->abort, p.dev_status)) {
       tc_fence_after();
       const bool direct = nsplit == 1;
       const float o_mul = (KV8 && !has_draft) ? p.v_scale : 1.0f;   // a quantised context tile: the V scale

@@ -1,22 +1,29 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace sdv {
 
 // Verify attention on tcgen05 tiles with TMA-staged pages (+ merge when num_splits > 1).
-constexpr int kTcMaxNQ = 96;    // query columns per CTA (heads-per-CTA x nodes, padded to 16)
 struct TcPlan {
   int hpc;      // query heads of a KV group handled by one CTA: 6, 3, 2 or 1
   int hparts;   // CTAs per (split, KV head): ceil(6 / hpc)
   int nq;       // query columns per CTA: hpc x max nodes rounded up to 16 (>= 32)
 };
+// bf16 caches: the ring-buffered kernel (attn_ring_kernel.cuh), up to 144 query columns per CTA.
+constexpr int kRingMaxNQ = 144;
+TcPlan ring_plan(int max_nodes);
+cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+// its sliding-window instances (attn_ring_win.cu)
+cudaError_t launch_ring_window(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
+                               const BatchDesc& bd, const TcPlan& pl, cudaStream_t st);
+// e4m3 caches (p.k_cache8 / p.v_cache8 with p.k_scale / p.v_scale): attn_tc_kernel.cuh, up to 96 columns.
+constexpr int kTcMaxNQ = 96;
 TcPlan tc_plan(int max_nodes);
 size_t tc_smem_bytes(int nq);
-int attn_tc_tile();
-cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
-// The same on e4m3 caches (p.k_cache8 / p.v_cache8 with p.k_scale / p.v_scale).
 cudaError_t launch_attn_tc8(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 
 // Log-sum-exp merge of the split partials into the bf16 output.
