@@ -23,16 +23,15 @@ PFN_cuTensorMapEncodeTiled_v12000 ring_encode_fn() {
 // The cache viewed as 4-D: x = dim within a 64-dim block (contiguous),
 // y = slot within an 8-slot half page (512 B apart), z = 64-dim block (128 B
 // apart), w = half page of one KV head ((page * 4 + head) * 2 + half, 4 KB
-// apart), with the 128-byte swizzle.  `blocks` = 4: a box is one page of one
-// head (8 KB: [half][block][8 slots][128 B], the V slot layout); `blocks` = 1:
-// a box is one 64-dim block of one page (2 KB: [half][8 slots][128 B], two
-// 8-row groups of a K slot).
-bool ring_map(CUtensorMap* map, const void* cache, int pool_pages, int blocks) {
+// apart), with the 128-byte swizzle.  A box of {64, 8, 4, 2} is one page of
+// one head (8 contiguous KB), landing as [half][block][8 slots][128 B]: two
+// 8-row groups of the group-major K tile or of a V page slot.
+bool ring_map(CUtensorMap* map, const void* cache, int pool_pages) {
   auto fn = ring_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {64, 8, 4, (cuuint64_t)pool_pages * kHkv * 2};
   cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, 128, (cuuint64_t)kDim * 2 * 8};
-  cuuint32_t box[4] = {64, 8, (cuuint32_t)blocks, 2};
+  cuuint32_t box[4] = {64, 8, 4, 2};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -56,7 +55,7 @@ TcPlan ring_plan(int max_nodes) {
 
 cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   CUtensorMap mk, mv;
-  if (!ring_map(&mk, p.k_cache, p.num_pool_pages, 1) || !ring_map(&mv, p.v_cache, p.num_pool_pages, 4))
+  if (!ring_map(&mk, p.k_cache, p.num_pool_pages) || !ring_map(&mv, p.v_cache, p.num_pool_pages))
     return cudaErrorInvalidValue;
   const TcPlan pl = ring_plan(bd.max_nodes);
   const cudaError_t e = p.window > 0 ? launch_ring_window(mk, mv, p, bd, pl, st)

@@ -1,6 +1,6 @@
 // Split-KV verify attention over bf16 pages, one CTA per (split, KV head):
-// every query head of the KV group in one tile, K and V streamed through
-// fine-grained shared-memory rings, accumulators in tensor memory (tcgen05).
+// every query head of the KV group in one tile, V streamed through a page
+// ring, accumulators in tensor memory (tcgen05).
 //
 // What it computes is the tree/causal-masked grouped-query attention of the
 // verify step: for sequence b, draft node j and query head h, softmax
@@ -20,26 +20,27 @@
 //   O^T[256 dim][NQ]     += V_tile^T[256][128 tok] . P^T[128 tok][NQ]
 //                           (two M = 128 halves of the dims; MN-major A and B)
 // In tensor memory: S^T in columns [0, NQ), O^T in [NQ, 3 NQ) (dims 0-127, then
-// 128-255; one dim per lane).  P^T is the bf16 tile the softmax writes: 64-column
-// atoms with the 128-byte swizzle, and for NQ = 144 a 16-column tail with the
-// 32-byte swizzle.
+// 128-255; one dim per lane).
 //
-// Rings.  K arrives in 16 KB slots, each one 64-dim block of a tile (one 2 KB
-// TMA box per page), and is released block by block as QK consumes it; V
-// arrives in 8 KB slots, one page each (one TMA box), released page by page as
-// PV consumes it (a page is one 16-token K-step of the PV product).  So while
-// the softmax works on tile i, the next tile's K blocks and this tile's
-// remaining V pages are already in flight, in whatever room the rings have.
+// Shared memory.  Q^T (NQ x 512 B) stays for the whole CTA.  K is one 64 KB
+// tile, loaded as eight 8 KB page boxes (contiguous in the cache) and released
+// as soon as QK has read it.  V pages (8 KB each) go through a ring of at least
+// a whole tile, released page by page as PV consumes them (a page is one
+// 16-token K-step of the PV product).  P^T holds half a tile: token rows 0-63
+// are written, multiplied (pages 0-3), then replaced by rows 64-127 (pages
+// 4-7); its 64-column atoms use the 128-byte swizzle, and for NQ = 144 a
+// 16-column tail the 32-byte swizzle.  Halving P^T is what leaves room for the
+// whole-tile V ring at NQ = 144.
 //
-// Warp roles (224 threads): warp 0 streams K, warp 6 streams V; warp 1
-// allocates tensor memory and one lane issues every tcgen05.mma, taking the
-// next QK block or the next PV page, whichever has its inputs; warps 2-5 (one
-// per tensor-memory lane quarter: thread = token row) run the online softmax
-// (running per-column maxima raised, with O and l rescaled, only when a score
-// exceeds them by more than 2^8) and write P^T, then in the epilogue (thread =
-// one dim of every query column) normalise and store the output rows.  Every
-// mbarrier wait is bounded; on expiry the kernel reports SD_DEV_TIMEOUT and
-// winds down.
+// Warp roles (256 threads): warp 0 streams K, warp 6 streams V; warp 1
+// allocates tensor memory and one lane issues the QK products, warp 7 one lane
+// the PV products, each blocking on exactly the barrier it needs next; warps
+// 2-5 (one per tensor-memory lane quarter: thread = token row) run the online
+// softmax (running per-column maxima raised, with O and l rescaled, only when
+// a score exceeds them by more than 2^8) and write P^T, then in the epilogue
+// (thread = one dim of every query column) normalise and store the output
+// rows.  Every mbarrier wait is bounded; on expiry the kernel reports
+// SD_DEV_TIMEOUT and winds down.
 #pragma once
 
 #include <cstddef>
@@ -54,11 +55,13 @@ namespace sdv {
 namespace {
 
 constexpr int kT = kTileTokens;        // tokens per tile
-constexpr int kRingThreads = 224;
-constexpr int kRWarpK = 0, kRWarpMma = 1, kRWarpV = 6;
-constexpr int kKBlkB = kT * 128;       // K slot: one 64-dim block of a tile, 16 groups of 8 rows x 128 B
-constexpr int kPAtomB = kT * 128;      // one 64-column atom of P^T (128 token rows x 128 B)
-constexpr int kPTailB = kT * 32;       // the 16-column tail of P^T (128 token rows x 32 B)
+constexpr int kRingThreads = 256;
+constexpr int kRWarpK = 0, kRWarpQK = 1, kRWarpV = 6, kRWarpPV = 7;
+constexpr int kComputeThreads = 192;   // warps 1-5 and 7 (they stage Q^T)
+constexpr int kKTileB = kT / 8 * kGroupB;   // the K tile: 16 groups of 8 rows x 4 dim blocks (64 KB)
+constexpr int kPRows = kT / 2;         // P^T holds half a tile: token rows 0-63, then 64-127
+constexpr int kPAtomB = kPRows * 128;  // one 64-column atom of P^T (64 token rows x 128 B)
+constexpr int kPTailB = kPRows * 32;   // the 16-column tail of P^T (64 token rows x 32 B)
 constexpr int kSmemMax = 232448;       // 227 KB of dynamic shared memory per CTA
 constexpr int kMaxStage = kRingMaxNQ + 2 * kMaxNodes;   // staging rows: Q^T + the draft block's K and V
 constexpr int kMaxBars = 44;
@@ -92,13 +95,12 @@ struct Ring {
   static constexpr int kQB = NQ * 512;                     // Q^T: 4 blocks of NQ rows x 128 B
   static constexpr int kPB = kPA * kPAtomB + (kTail ? kPTailB : 0);
   static constexpr int kFixed = kQB + kPB + (int)sizeof(RSmall<kCols>);
-  static constexpr int kBudget = kSmemMax - kFixed;
-  static constexpr int RK = kBudget / 2 / kKBlkB < 4 ? 4 : (kBudget / 2 / kKBlkB > 8 ? 8 : kBudget / 2 / kKBlkB);
-  static constexpr int RV0 = (kBudget - RK * kKBlkB) / kPageB;
-  static constexpr int RV = RV0 > 16 ? 16 : RV0;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 5;
-  static constexpr size_t kSmem = (size_t)kQB + (size_t)RK * kKBlkB + (size_t)RV * kPageB + kPB + sizeof(RSmall<kCols>);
-  static_assert(RV >= 4 && RK >= 4, "the draft tile needs four K blocks and four V pages");
+  static constexpr int kBudget = kSmemMax - kFixed - kKTileB;
+  static constexpr int RV0 = kBudget / kPageB;
+  static constexpr int RV = RV0 > 12 ? 12 : RV0;
+  static constexpr int kNumBars = 2 * RV + 12;
+  static constexpr size_t kSmem = (size_t)kQB + (size_t)kKTileB + (size_t)RV * kPageB + kPB + sizeof(RSmall<kCols>);
+  static_assert(RV >= 8, "the V ring holds at least a whole tile");
   static_assert(kNumBars <= kMaxBars, "barrier array too small");
   static_assert(kSmem <= (size_t)kSmemMax, "shared memory over 227 KB");
   static_assert(kPB >= kMaxStage * 16, "the staging table lives in the P^T region");
@@ -108,22 +110,24 @@ struct Ring {
 // WIN: compiled with the sliding-window paths (band masks, depths).
 template <int NQ, bool WIN>
 __global__ void __launch_bounds__(kRingThreads, 1)
-attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vp,
+attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
   using R = Ring<NQ>;
-  constexpr int NG = R::NG, RK = R::RK, RV = R::RV, NQA = R::NQA, NPA = R::kPA;
+  constexpr int NG = R::NG, RV = R::RV, NQA = R::NQA, NPA = R::kPA;
   constexpr bool TAIL = R::kTail;
   constexpr uint32_t kColS = 0, kColO = NQ;   // tensor-memory columns: S^T, then O^T (two halves of NQ)
-  // Barriers: K slot full / empty, V slot full / empty, then the tile-level ones.
-  constexpr int B_KF = 0, B_KE = RK, B_VF = 2 * RK, B_VE = 2 * RK + RV;
-  constexpr int S_FULL = 2 * RK + 2 * RV, S_FREE = S_FULL + 1, P_FULL = S_FULL + 2, O_DONE = S_FULL + 3,
-                GROUP = S_FULL + 4;
+  // Barriers: V slot full / empty, then the tile-level ones.  CSUM_A / CSUM_B:
+  // the warps of a half tile have read their P^T rows back (column sums).
+  constexpr int B_VF = 0, B_VE = RV;
+  constexpr int K_FULL = 2 * RV, K_EMPTY = K_FULL + 1, S_FULL = K_FULL + 2, S_FREE = K_FULL + 3,
+                P_FULL_A = K_FULL + 4, O_HALF = K_FULL + 5, P_FULL_B = K_FULL + 6, O_DONE = K_FULL + 7,
+                CSUM_A = K_FULL + 8, CSUM_B = K_FULL + 9, GROUP = K_FULL + 10;
   // No static shared memory: the dynamic window starts on a 1024-byte boundary
   // (the 128-byte swizzle atoms need it).
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   uint8_t* sQ = dyn_smem;
   uint8_t* sK = sQ + R::kQB;
-  uint8_t* sV = sK + RK * kKBlkB;
+  uint8_t* sV = sK + kKTileB;
   uint8_t* sP = sV + RV * kPageB;
   uint8_t* sPt = sP + NPA * kPAtomB;
   using Sm = RSmall<R::kCols>;
@@ -161,12 +165,12 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
   }
   // The draft CTA (split 0) runs to the end in every case: it takes its tensor
   // memory before the wait (no global memory involved).
-  if (s == 0 && warp == kRWarpMma) {
+  if (s == 0 && warp == kRWarpQK) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (producer && lane == 0)
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kRWarpV ? &tm_vp : &tm_kb))
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kRWarpV ? &tm_v : &tm_k))
                  : "memory");
   if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -202,7 +206,8 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
     for (int i = 0; i < R::kNumBars; ++i) {
-      const uint32_t cnt = (i == S_FREE || i == P_FULL || i == GROUP) ? 4u : 1u;
+      const uint32_t cnt = (i == S_FREE || i == P_FULL_A || i == GROUP) ? 4u
+                           : (i == P_FULL_B || i == CSUM_A || i == CSUM_B) ? 2u : 1u;
       mbar_init(smem_u32(&sm->bar[i]), cnt);
     }
     sm->abort = 0;
@@ -226,9 +231,8 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
 
   // Staging of the operands that do not come by TMA, by `nthr` threads (index
   // t): Q^T (K-major, block-major; column q = node * hpc + head-in-part, zeros
-  // past `rows`) and, in the draft CTA, the draft block: K rows into the four
-  // K slots (slot = 64-dim block; node t = token row t) and V rows into the
-  // first V slots (page layout).  A row table (source, destination, block
+  // past `rows`) and, in the draft CTA, the draft block: K rows into the K tile
+  // and V rows into the first V slots (both group-major; node t = token row t).  A row table (source, destination, block
   // stride) is built first, then one pass of 16-byte copies with up to 16
   // loads in flight per thread; the last round repeats the final chunk instead
   // of branching, so the unrolled copies stay independent.
@@ -247,20 +251,15 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
         const bool is_v = r >= NQ + n_nodes;
         const int tok = r - NQ - (is_v ? n_nodes : 0);
         src = (is_v ? p.v_new : p.k_new) + ((size_t)(q0 + tok) * kHkv + g) * kDim;
-        if (is_v) {
-          dst = (uint32_t)(sV - dyn_smem) + (tok >> 3) * kGroupB + (tok & 7) * 128;
-          blk = 1024;
-        } else {
-          dst = (uint32_t)(sK - dyn_smem) + (tok >> 3) * 1024 + (tok & 7) * 128;
-          blk = kKBlkB;
-        }
+        dst = (uint32_t)((is_v ? sV : sK) - dyn_smem) + (tok >> 3) * kGroupB + (tok & 7) * 128;
+        blk = 1024;
       }
       rsrc[r] = src;
       rdst[r] = dst;
       rblk[r] = blk;
     }
     if (all_warps) __syncthreads();
-    else asm volatile("bar.sync 3, 160;" ::: "memory");   // the five compute warps
+    else asm volatile("bar.sync 3, 192;" ::: "memory");   // the compute warps
     constexpr int U = 16;
     const int tasks = n_stage * 32;
     for (int t0 = t; t0 - t < tasks; t0 += nthr * U) {
@@ -300,7 +299,6 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
     int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
     int slot = 0, fills = 0;
     uint32_t ph = 0;
-    const int ring = is_k ? RK : RV;
     bool ok = true;
     for (int i = 0; i < n_ctx && ok; ++i) {
       const int t0 = ctx_begin + i * kT;
@@ -315,32 +313,28 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
         bad = true;
       }
       if (is_k) {
-        // K: four 64-dim blocks per tile, each a slot of eight 2 KB boxes.
-        // Pages past the context are not loaded (their rows are masked);
-        // pages with an id out of range are zeros.
+        // K: the whole tile, one 8 KB box per page.  Pages past the context are
+        // not loaded (their rows are masked); pages with an id out of range
+        // are zeros.
+        if (lane == 0) ok = mbar_wait(bar(K_EMPTY), (uint32_t)(i & 1) ^ 1u, &sm->abort, p.dev_status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
         const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page >= 0);
         const uint32_t zero_mask = __ballot_sync(0xffffffffu, bad);
-        for (int kb = 0; kb < 4; ++kb) {
-          if (lane == 0) ok = mbar_wait(bar(B_KE + slot), ph ^ 1u, &sm->abort, p.dev_status);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          uint8_t* dst = sK + slot * kKBlkB;
-          if (zero_mask != 0u) {
-            for (uint32_t zm = zero_mask; zm != 0u; zm &= zm - 1u) {
-              const int pi = __ffs(zm) - 1;
-              for (int e = lane; e < 2048 / 16; e += 32)
-                *reinterpret_cast<uint4*>(dst + pi * 2048 + e * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_async_smem();
+        if (zero_mask != 0u) {
+          for (uint32_t zm = zero_mask; zm != 0u; zm &= zm - 1u) {
+            const int pi = __ffs(zm) - 1;
+            for (int e = lane; e < kPageB / 16; e += 32)
+              *reinterpret_cast<uint4*>(sK + pi * kPageB + e * 16) = make_uint4(0, 0, 0, 0);
           }
-          __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_KF + slot), (uint32_t)__popc(tma_mask) * 2048u);
-          __syncwarp();
-          if ((tma_mask >> lane) & 1u)
-            tma_load_kblk(smem_u32(dst + lane * 2048), &tm_kb, kb, (page * kHkv + g) * 2, bar(B_KF + slot));
-          ++fills;
-          if (++slot == ring) { slot = 0; ph ^= 1u; }
+          fence_async_smem();
         }
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(bar(K_FULL), (uint32_t)__popc(tma_mask) * (uint32_t)kPageB);
+        __syncwarp();
+        if ((tma_mask >> lane) & 1u)
+          tma_load_page(smem_u32(sK + lane * kPageB), &tm_k, (page * kHkv + g) * 2, bar(K_FULL));
+        ++fills;
       } else {
         // V: the tile's pages up to the last valid token, one slot each.  A
         // page goes by TMA when it is in range and all its 16 tokens are valid;
@@ -364,10 +358,10 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
           __syncwarp();
           if (lane == 0) {
             mbar_expect_tx(bar(B_VF + slot), full ? (uint32_t)kPageB : 0u);
-            if (full) tma_load_page(smem_u32(dst), &tm_vp, (pg * kHkv + g) * 2, bar(B_VF + slot));
+            if (full) tma_load_page(smem_u32(dst), &tm_v, (pg * kHkv + g) * 2, bar(B_VF + slot));
           }
           ++fills;
-          if (++slot == ring) { slot = 0; ph ^= 1u; }
+          if (++slot == RV) { slot = 0; ph ^= 1u; }
         }
       }
       // early context loads: the later slots free up only as the compute warps (which wait) progress
@@ -377,35 +371,36 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
     // After an abort no copy may still be landing when the CTA ends: wait,
     // bounded, for the last fill of every slot.
     if (lane == 0 && *(volatile int*)&sm->abort) {
-      for (int j = 0; j < ring && j < fills; ++j) {
-        const uint32_t parity = j < slot ? ph : ph ^ 1u;   // the last fill of slot j
+      const int nslots = is_k ? 1 : RV;
+      for (int j = 0; j < nslots && j < fills; ++j) {
+        const uint32_t parity = is_k ? (uint32_t)((fills - 1) & 1) : (j < slot ? ph : ph ^ 1u);   // the last fill
         const long long t0 = clock64();
-        while (!mbar_test(bar((is_k ? B_KF : B_VF) + j), parity) && clock64() - t0 < kWaitCycles) {
+        while (!mbar_test(bar(is_k ? K_FULL : B_VF + j), parity) && clock64() - t0 < kWaitCycles) {
         }
       }
     }
   } else {
-  // ---------------------------------------------------------------- compute warps (1-5)
-  // While the producers fetch the first tiles, these five warps stage Q^T and
+  // ---------------------------------------------------------------- compute warps (1-5, 7)
+  // While the producers fetch the first tiles, these six warps stage Q^T and
   // allocate tensor memory.
   {
-    const int ct = tid - 32;
+    const int ct = warp == kRWarpPV ? 160 + lane : tid - 32;
     if (early) {
       // tensor memory first (no global memory), then the wait for the previous kernel
-      if (warp == kRWarpMma) {
+      if (warp == kRWarpQK) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       if (W > 0)
-        for (int j = ct; j < n_nodes; j += 5 * 32) sm->par[j] = p.parents[q0 + j];
+        for (int j = ct; j < n_nodes; j += kComputeThreads) sm->par[j] = p.parents[q0 + j];
     }
-    if (!has_draft) stage_operands(ct, 5 * 32, false);
+    if (!has_draft) stage_operands(ct, kComputeThreads, false);
     if (W > 0) {
       // oldest visible context position of each query column: L + depth(node) - W + 1
       // (padding columns take the root's; an invalid parent chain stops the walk)
       const float inv_hpc = 1.0f / (float)hpc;
-      for (int q = ct; q < R::kCols; q += 5 * 32) {
+      for (int q = ct; q < R::kCols; q += kComputeThreads) {
         int d = 0;
         if (q < rows) {
           for (int u = __float2int_rz(((float)q + 0.5f) * inv_hpc); u > 0 && d < kMaxNodes; ++d) {
@@ -417,95 +412,78 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
         sm->lo_col[q] = L + d - W + 1;
       }
     }
-    if (warp == kRWarpMma && !early && s != 0) {
+    if (warp == kRWarpQK && !early && s != 0) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm->tmem)));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     fence_async_smem();
     tc_fence_before();
-    asm volatile("bar.sync 1, 160;" ::: "memory");   // the five compute warps, all arrive unconditionally
+    asm volatile("bar.sync 1, 192;" ::: "memory");   // the compute warps, all arrive unconditionally
     tc_fence_after();
   }
   const uint32_t tmem = sm->tmem;
-  if (warp == kRWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  if (warp == kRWarpQK) {
+    // ------------------------------------------------------------ QK issuer
+    // QK of tile i once its K tile has landed and the softmax has read S^T of tile i - 1.
     if (lane == 0) {
       constexpr uint32_t kIdQK = f16_idesc(128, NQ, 0, 0);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK);
+      for (int i = 0; i < n_tiles; ++i) {
+        if (i > 0 && !mbar_wait(bar(S_FREE), (uint32_t)(i - 1) & 1u, &sm->abort, p.dev_status)) break;
+        if (!has_draft && !mbar_wait(bar(K_FULL), (uint32_t)i & 1u, &sm->abort, p.dev_status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kDim / 16; ++kk) {
+          // A = K, K-major: 8-row groups 4 KB apart, 64-dim blocks 1 KB apart, 32 bytes per 16-dim step;
+          // B = Q^T, K-major, block-major: 64-dim blocks NQ * 128 B apart, 8-row groups 1 KB apart
+          const uint32_t off = (kk & 3) * 32;
+          umma(tmem + kColS, sw128_desc(k_addr + (kk >> 2) * 1024 + off, 16, kGroupB),
+               sw128_desc(q_addr + (kk >> 2) * NQ * 128 + off, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        }
+        if (!has_draft) umma_commit(bar(K_EMPTY));
+        umma_commit(bar(S_FULL));
+      }
+    }
+  } else if (warp == kRWarpPV) {
+    // ------------------------------------------------------------ PV issuer
+    // PV of tile i, one page (16 tokens) at a time, in two halves: pages 0-3
+    // once P^T holds token rows 0-63 (P_FULL_A), then pages 4-7 once the
+    // softmax has replaced them by rows 64-127 (P_FULL_B).
+    if (lane == 0) {
       constexpr uint32_t kIdPV = f16_idesc(128, NQA, 1, 1);
       constexpr uint32_t kIdPVt = f16_idesc(128, 16, 1, 1);
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint32_t p_addr = smem_u32(sP), pt_addr = smem_u32(sPt);
-      int ks = 0, vs = 0;          // ring slots
-      uint32_t kph = 0, vph = 0;   // their fill parities
-      int qk_i = 0, qk_b = 0;      // QK: tile, next 64-dim block
-      int pv_i = 0, pv_j = 0;      // PV: tile, next page
-      int pv_pages = (tile_valid(0) + kPage - 1) / kPage;
-      long long idle_since = clock64();
-      while (pv_i < n_tiles) {
-        bool progressed = false;
-        // QK, one 64-dim block: the block's slot has landed, and for a tile's
-        // first block the softmax has read the previous S^T
-        if (qk_i < n_tiles) {
-          const bool s_ok = qk_b > 0 || qk_i == 0 || mbar_test(bar(S_FREE), (uint32_t)(qk_i - 1) & 1u);
-          const bool k_ok = has_draft || mbar_test(bar(B_KF + ks), kph);
-          if (s_ok && k_ok) {
-            tc_fence_after();
-            const uint32_t ka = k_addr + (uint32_t)ks * kKBlkB;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // A = K block, K-major: 8-row groups 1 KB apart, 32 bytes per 16-dim step;
-              // B = Q^T block qk_b, K-major: 8-row groups 1 KB apart
-              umma(tmem + kColS, sw128_desc(ka + k * 32, 16, 1024),
-                   sw128_desc(q_addr + (uint32_t)qk_b * NQ * 128 + k * 32, 16, 1024), kIdQK,
-                   (qk_b | k) != 0 ? 1u : 0u);
+      const uint32_t v_addr = smem_u32(sV), p_addr = smem_u32(sP), pt_addr = smem_u32(sPt);
+      int vs = 0;
+      uint32_t vph = 0;
+      bool ok = true;
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int npg = (tile_valid(i) + kPage - 1) / kPage;
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = mbar_wait(bar(half ? P_FULL_B : P_FULL_A), (uint32_t)i & 1u, &sm->abort, p.dev_status);
+          if (!ok) break;
+          tc_fence_after();
+          for (int j = 4 * half; j < min(npg, 4 * half + 4); ++j) {
+            if (!has_draft) {
+              ok = mbar_wait(bar(B_VF + vs), vph, &sm->abort, p.dev_status);
+              if (!ok) break;
+              tc_fence_after();
             }
-            if (!has_draft) umma_commit(bar(B_KE + ks));
-            if (++ks == RK) { ks = 0; kph ^= 1u; }
-            if (++qk_b == 4) {
-              umma_commit(bar(S_FULL));
-              qk_b = 0;
-              ++qk_i;
-            }
-            progressed = true;
-          }
-        }
-        // PV, one page (16 tokens): P^T of the tile is written, the page has landed
-        if (pv_i < qk_i) {
-          const bool p_ok = pv_j > 0 || mbar_test(bar(P_FULL), (uint32_t)pv_i & 1u);
-          const bool v_ok = has_draft || mbar_test(bar(B_VF + vs), vph);
-          if (p_ok && v_ok) {
-            tc_fence_after();
             const uint32_t va = v_addr + (uint32_t)vs * kPageB;
-            const uint32_t acc = (pv_i > 0 || pv_j > 0) ? 1u : 0u;
+            const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
+            const uint32_t prow = (uint32_t)(j & 3) * 16;   // the page's first row in the half tile
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
               // A = V^T, dims mb*128.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart;
-              // B = P^T rows 16 pv_j.., MN-major: 64-column atoms 16 KB apart, 8-token groups 1 KB apart
+              // B = P^T rows of the page, MN-major: 64-column atoms 8 KB apart, 8-token groups 1 KB apart
               const uint64_t a = sw128_desc(va + mb * 2048, 1024, kGroupB);
-              umma(tmem + kColO + mb * NQ, a, sw128_desc(p_addr + pv_j * 2048, kPAtomB, 1024), kIdPV, acc);
+              umma(tmem + kColO + mb * NQ, a, sw128_desc(p_addr + prow * 128, kPAtomB, 1024), kIdPV, acc);
               if (TAIL)   // columns 128-143: 32-byte rows, 8-token groups 256 B apart
-                umma(tmem + kColO + mb * NQ + 128, a, sw32_desc(pt_addr + pv_j * 512, kPTailB, 256), kIdPVt, acc);
+                umma(tmem + kColO + mb * NQ + 128, a, sw32_desc(pt_addr + prow * 32, kPTailB, 256), kIdPVt, acc);
             }
             if (!has_draft) umma_commit(bar(B_VE + vs));
             if (++vs == RV) { vs = 0; vph ^= 1u; }
-            if (++pv_j == pv_pages) {
-              umma_commit(bar(O_DONE));
-              pv_j = 0;
-              ++pv_i;
-              if (pv_i < n_tiles) pv_pages = (tile_valid(pv_i) + kPage - 1) / kPage;
-            }
-            progressed = true;
           }
-        }
-        if (progressed) {
-          idle_since = clock64();
-        } else {
-          if (clock64() - idle_since > kWaitCycles || *(volatile int*)&sm->abort) {
-            sm->abort = 1;
-            report(p.dev_status, SD_DEV_TIMEOUT);
-            break;
-          }
-          __nanosleep(20);
+          if (ok) umma_commit(bar(half ? O_DONE : O_HALF));
         }
       }
     }
@@ -721,29 +699,46 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
         }
         tmem_wait_st();
       }
+      // P^T holds half a tile: the warps of token rows 0-63 (lane quarters 0
+      // and 1) write theirs first; the warps of rows 64-127 signal that their
+      // rescale (if any) is done, wait until the PV product and the first
+      // warps' column sums have read rows 0-63, then write theirs into the same
+      // rows of P^T.  The next tile's first warps wait in turn for the PV
+      // product and these warps' column sums.
+      const bool second_half = quarter >= 2;
+      const int hr = row & (kPRows - 1);   // row within the half tile
+      if (second_half) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_FULL_A));
+        if (!mbar_spin(bar(O_HALF), (uint32_t)i & 1u, &sm->abort, p.dev_status)) break;
+        if (!mbar_spin(bar(CSUM_A), (uint32_t)i & 1u, &sm->abort, p.dev_status)) break;
+      } else if (i > 0) {
+        if (!mbar_spin(bar(CSUM_B), (uint32_t)(i - 1) & 1u, &sm->abort, p.dev_status)) break;
+      }
       // P^T row of this token: 64-column atoms, then the tail
 #pragma unroll
       for (int ch = 0; ch < NQ / 8; ++ch) {
         const uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
         if (ch < NQA / 8) {
-          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kPAtomB + p_off(row, ch & 7)) = w;
+          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kPAtomB + p_off(hr, ch & 7)) = w;
         } else {
           const int tc = ch - NQA / 8;   // 0 or 1
-          *reinterpret_cast<uint4*>(sPt + row * 32 + ((tc ^ ((row >> 2) & 1)) << 4)) = w;
+          *reinterpret_cast<uint4*>(sPt + hr * 32 + ((tc ^ ((hr >> 2) & 1)) << 4)) = w;
         }
       }
       tc_fence_before();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(P_FULL));
-      // Column sums of this tile's P from the rows this warp just wrote, while
-      // the PV product runs (the next tile overwrites P^T only after it ends).
+      if (lane == 0) mbar_arrive(bar(second_half ? P_FULL_B : P_FULL_A));
+      // Column sums of this tile's P from the rows this warp just wrote (the
+      // same bf16 weights the PV product multiplies V with), while PV runs.
 #pragma unroll
       for (int a = 0; a < NPA; ++a) {
         if (a * 64 + cs_chunk * 8 < NQA) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int r = quarter * 32 + (lane >> 3) + 4 * k;
+            const int r = (quarter & 1) * 32 + (lane >> 3) + 4 * k;
             const uint4 pv = *reinterpret_cast<const uint4*>(sP + a * kPAtomB + p_off(r, cs_chunk));
             const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
@@ -758,7 +753,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
       if (TAIL) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int r = quarter * 32 + (lane >> 1) + 16 * k;
+          const int r = (quarter & 1) * 32 + (lane >> 1) + 16 * k;
           const uint4 pv = *reinterpret_cast<const uint4*>(sPt + r * 32 + (((lane & 1) ^ ((r >> 2) & 1)) << 4));
           const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
@@ -769,6 +764,8 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(second_half ? CSUM_B : CSUM_A));
     }
 
     // ------------------------------------------------------------ epilogue
@@ -870,7 +867,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_kb, const __grid_constan
   tc_fence_before();
   }  // compute warps
   __syncthreads();
-  if (warp == kRWarpMma) {
+  if (warp == kRWarpQK) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm->tmem));
   }
