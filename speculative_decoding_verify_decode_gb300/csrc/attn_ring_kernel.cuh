@@ -60,8 +60,6 @@ constexpr int kRWarpK = 0, kRWarpQK = 1, kRWarpV = 6, kRWarpPV = 7;
 constexpr int kComputeThreads = 192;   // warps 1-5 and 7 (they stage Q^T)
 constexpr int kKTileB = kT / 8 * kGroupB;   // the K tile: 16 groups of 8 rows x 4 dim blocks (64 KB)
 constexpr int kPRows = kT / 2;         // P^T holds half a tile: token rows 0-63, then 64-127
-constexpr int kPAtomB = kPRows * 128;  // one 64-column atom of P^T (64 token rows x 128 B)
-constexpr int kPTailB = kPRows * 32;   // the 16-column tail of P^T (64 token rows x 32 B)
 constexpr int kSmemMax = 232448;       // 227 KB of dynamic shared memory per CTA
 constexpr int kMaxStage = kRingMaxNQ + 2 * kMaxNodes;   // staging rows: Q^T + the draft block's K and V
 constexpr int kMaxBars = 44;
@@ -89,15 +87,17 @@ template <int NQ>
 struct Ring {
   static constexpr int NG = (NQ + 31) / 32;               // 32-column groups
   static constexpr int kCols = NG * 32;
-  static constexpr bool kTail = NQ > 128;                  // columns 128.. in the 32-byte-swizzle tail
-  static constexpr int NQA = kTail ? 128 : NQ;             // columns in 64-column atoms
-  static constexpr int kPA = (NQA + 63) / 64;
+  // P^T: 64-column atoms with the 128-byte swizzle, or (NQ > 128) 16-column
+  // atoms with the 32-byte swizzle, so that one product with N = NQ reads it.
+  static constexpr bool kSW32 = NQ > 128;
+  static constexpr int kPAtom = kSW32 ? kPRows * 32 : kPRows * 128;   // bytes per atom
+  static constexpr int kPA = kSW32 ? NQ / 16 : (NQ + 63) / 64;         // atoms
   static constexpr int kQB = NQ * 512;                     // Q^T: 4 blocks of NQ rows x 128 B
-  static constexpr int kPB = kPA * kPAtomB + (kTail ? kPTailB : 0);
+  static constexpr int kPB = kPA * kPAtom;
   static constexpr int kFixed = kQB + kPB + (int)sizeof(RSmall<kCols>);
   static constexpr int kBudget = kSmemMax - kFixed - kKTileB;
   static constexpr int RV0 = kBudget / kPageB;
-  static constexpr int RV = RV0 > 12 ? 12 : RV0;
+  static constexpr int RV = RV0 > 12 ? 12 : RV0;          // V slots, one page each
   static constexpr int kNumBars = 2 * RV + 12;
   static constexpr size_t kSmem = (size_t)kQB + (size_t)kKTileB + (size_t)RV * kPageB + kPB + sizeof(RSmall<kCols>);
   static_assert(RV >= 8, "the V ring holds at least a whole tile");
@@ -113,8 +113,11 @@ __global__ void __launch_bounds__(kRingThreads, 1)
 attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
   using R = Ring<NQ>;
-  constexpr int NG = R::NG, RV = R::RV, NQA = R::NQA, NPA = R::kPA;
-  constexpr bool TAIL = R::kTail;
+  constexpr int NG = R::NG, RV = R::RV;
+  constexpr bool SW32 = R::kSW32;
+  constexpr int kPAtomB = R::kPAtom;
+  // column sums: 64-column atoms (a lane: 8 columns of each), or 16-column atoms (a lane: up to three)
+  constexpr int NCS = SW32 ? 3 : R::kPA;
   constexpr uint32_t kColS = 0, kColO = NQ;   // tensor-memory columns: S^T, then O^T (two halves of NQ)
   // Barriers: V slot full / empty, then the tile-level ones.  CSUM_A / CSUM_B:
   // the warps of a half tile have read their P^T rows back (column sums).
@@ -129,7 +132,6 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   uint8_t* sK = sQ + R::kQB;
   uint8_t* sV = sK + kKTileB;
   uint8_t* sP = sV + RV * kPageB;
-  uint8_t* sPt = sP + NPA * kPAtomB;
   using Sm = RSmall<R::kCols>;
   Sm* sm = reinterpret_cast<Sm*>(sP + R::kPB);
   // The staging table of the prologue (row source, destination, block stride)
@@ -297,8 +299,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int n_ctx = has_draft ? 0 : n_tiles;
     const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
     int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
-    int slot = 0, fills = 0;
-    uint32_t ph = 0;
+    int fills = 0;           // K tiles, or V pages, issued so far (V page f goes to ring slot f % RV)
     bool ok = true;
     for (int i = 0; i < n_ctx && ok; ++i) {
       const int t0 = ctx_begin + i * kT;
@@ -336,33 +337,45 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           tma_load_page(smem_u32(sK + lane * kPageB), &tm_k, (page * kHkv + g) * 2, bar(K_FULL));
         ++fills;
       } else {
-        // V: the tile's pages up to the last valid token, one slot each.  A
-        // page goes by TMA when it is in range and all its 16 tokens are valid;
-        // otherwise plain loads, zero past the context (P is 0 there, but 0
-        // times stale data could be NaN).
+        // V: the tile's pages up to the last valid token, one ring slot each,
+        // in two groups of four (pages 0-3 free up as PV consumes the previous
+        // tile's first half, pages 4-7 with its second half).  Lane j waits for
+        // the slot of page j; then the group's lanes issue their boxes
+        // together, as one warp instruction: boxes issued one thread after
+        // another cannot keep enough bytes in flight.  A page goes by TMA when
+        // it is in range and all its 16 tokens are valid; otherwise the warp
+        // copies it with plain loads, zero past the context (P is 0 there, but
+        // 0 times stale data could be NaN).
         const int npg = (valid + kPage - 1) / kPage;
-        for (int j = 0; j < npg; ++j) {
-          if (lane == 0) ok = mbar_wait(bar(B_VE + slot), ph ^ 1u, &sm->abort, p.dev_status);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int myslot = (fills + lane) % RV;
+        const uint32_t myph = (uint32_t)((fills + lane) / RV) & 1u;
+        const bool full = lane < npg && page >= 0 && (lane + 1) * kPage <= valid;
+        for (int grp = 0; grp < 2 && grp * 4 < npg && ok; ++grp) {
+          const bool mine = lane >= 4 * grp && lane < 4 * grp + 4 && lane < npg;
+          bool lane_ok = true;
+          if (mine) lane_ok = mbar_wait(bar(B_VE + myslot), myph ^ 1u, &sm->abort, p.dev_status);
+          ok = __all_sync(0xffffffffu, lane_ok);
           if (!ok) break;
-          const int pg = __shfl_sync(0xffffffffu, page, j);
-          const bool full = pg >= 0 && (j + 1) * kPage <= valid;
-          uint8_t* dst = sV + slot * kPageB;
-          if (!full) {
-            stage_rows(dst, 0, kPage, [&](int r) -> const __nv_bfloat16* {
-              return (pg >= 0 && j * kPage + r < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + r) * kDim
-                                                        : nullptr;
-            }, lane, 32);
-            fence_async_smem();
+          if (mine && full) {
+            mbar_expect_tx(bar(B_VF + myslot), (uint32_t)kPageB);
+            tma_load_page(smem_u32(sV + myslot * kPageB), &tm_v, (page * kHkv + g) * 2, bar(B_VF + myslot));
           }
           __syncwarp();
-          if (lane == 0) {
-            mbar_expect_tx(bar(B_VF + slot), full ? (uint32_t)kPageB : 0u);
-            if (full) tma_load_page(smem_u32(dst), &tm_v, (pg * kHkv + g) * 2, bar(B_VF + slot));
-          }
-          ++fills;
-          if (++slot == RV) { slot = 0; ph ^= 1u; }
         }
+        if (!ok) break;
+        for (uint32_t part = __ballot_sync(0xffffffffu, lane < npg && !full); part != 0u; part &= part - 1u) {
+          const int j = __ffs(part) - 1;
+          const int pg = __shfl_sync(0xffffffffu, page, j);
+          const int sj = (fills + j) % RV;
+          stage_rows(sV + sj * kPageB, 0, kPage, [&](int r) -> const __nv_bfloat16* {
+            return (pg >= 0 && j * kPage + r < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + r) * kDim
+                                                      : nullptr;
+          }, lane, 32);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_VF + sj));
+        }
+        fills += npg;
       }
       // early context loads: the later slots free up only as the compute warps (which wait) progress
       if (early && i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -373,7 +386,8 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (lane == 0 && *(volatile int*)&sm->abort) {
       const int nslots = is_k ? 1 : RV;
       for (int j = 0; j < nslots && j < fills; ++j) {
-        const uint32_t parity = is_k ? (uint32_t)((fills - 1) & 1) : (j < slot ? ph : ph ^ 1u);   // the last fill
+        const int last = j + (fills - 1 - j) / nslots * nslots;   // the last fill of slot j
+        const uint32_t parity = (uint32_t)(last / nslots) & 1u;
         const long long t0 = clock64();
         while (!mbar_test(bar(is_k ? K_FULL : B_VF + j), parity) && clock64() - t0 < kWaitCycles) {
         }
@@ -450,40 +464,44 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // once P^T holds token rows 0-63 (P_FULL_A), then pages 4-7 once the
     // softmax has replaced them by rows 64-127 (P_FULL_B).
     if (lane == 0) {
-      constexpr uint32_t kIdPV = f16_idesc(128, NQA, 1, 1);
-      constexpr uint32_t kIdPVt = f16_idesc(128, 16, 1, 1);
-      const uint32_t v_addr = smem_u32(sV), p_addr = smem_u32(sP), pt_addr = smem_u32(sPt);
-      int vs = 0;
-      uint32_t vph = 0;
+      constexpr uint32_t kIdPV = f16_idesc(128, NQ, 1, 1);
+      const uint32_t v_addr = smem_u32(sV), p_addr = smem_u32(sP);
+      int fills = 0;   // V pages consumed so far (page f in ring slot f % RV)
       bool ok = true;
       for (int i = 0; i < n_tiles && ok; ++i) {
         const int npg = (tile_valid(i) + kPage - 1) / kPage;
         for (int half = 0; half < 2 && ok; ++half) {
           ok = mbar_wait(bar(half ? P_FULL_B : P_FULL_A), (uint32_t)i & 1u, &sm->abort, p.dev_status);
           if (!ok) break;
+          const int nh = min(4, npg - 4 * half);   // pages of this half (none: an empty second half)
           tc_fence_after();
-          for (int j = 4 * half; j < min(npg, 4 * half + 4); ++j) {
+          for (int jj = 0; jj < nh && ok; ++jj) {
+            // each page as soon as it has landed
+            const int slot = has_draft ? 4 * half + jj : fills % RV;
             if (!has_draft) {
-              ok = mbar_wait(bar(B_VF + vs), vph, &sm->abort, p.dev_status);
+              ok = mbar_wait(bar(B_VF + slot), (uint32_t)(fills / RV) & 1u, &sm->abort, p.dev_status);
               if (!ok) break;
               tc_fence_after();
             }
-            const uint32_t va = v_addr + (uint32_t)vs * kPageB;
-            const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
-            const uint32_t prow = (uint32_t)(j & 3) * 16;   // the page's first row in the half tile
+            const uint32_t va = v_addr + (uint32_t)slot * kPageB;
+            const uint32_t acc = (i > 0 || half > 0 || jj > 0) ? 1u : 0u;
+            const uint32_t prow = (uint32_t)jj * 16;   // the page's first row in the half tile
 #pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
               // A = V^T, dims mb*128.., MN-major: 64-dim atoms 1 KB apart, 8-token groups 4 KB apart;
-              // B = P^T rows of the page, MN-major: 64-column atoms 8 KB apart, 8-token groups 1 KB apart
+              // B = P^T rows of the page, MN-major: column atoms kPAtomB apart, 8-token groups one atom row group apart
               const uint64_t a = sw128_desc(va + mb * 2048, 1024, kGroupB);
-              umma(tmem + kColO + mb * NQ, a, sw128_desc(p_addr + prow * 128, kPAtomB, 1024), kIdPV, acc);
-              if (TAIL)   // columns 128-143: 32-byte rows, 8-token groups 256 B apart
-                umma(tmem + kColO + mb * NQ + 128, a, sw32_desc(pt_addr + prow * 32, kPTailB, 256), kIdPVt, acc);
+              const uint64_t bd = SW32 ? sw32_desc(p_addr + prow * 32, kPAtomB, 256)
+                                       : sw128_desc(p_addr + prow * 128, kPAtomB, 1024);
+              umma(tmem + kColO + mb * NQ, a, bd, kIdPV, acc);
             }
-            if (!has_draft) umma_commit(bar(B_VE + vs));
-            if (++vs == RV) { vs = 0; vph ^= 1u; }
+            if (!has_draft) {
+              umma_commit(bar(B_VE + slot));
+              ++fills;
+            }
           }
-          if (ok) umma_commit(bar(half ? O_DONE : O_HALF));
+          if (!ok) break;
+          umma_commit(bar(half ? O_DONE : O_HALF));
         }
       }
     }
@@ -510,19 +528,20 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       }
     };
     // Column sums of P from the bf16 tile this warp wrote (the same rounded
-    // weights the PV product multiplies V with).  Atoms: lane L sums columns
-    // 64a + 8(L%8) .. +7 over token rows 32 quarter + L/8 + 4k, k < 8.  Tail:
-    // columns 128 + 8(L%2) .. +7 over rows 32 quarter + L/2 + 16k, k < 2.  The
-    // lanes and the four warps are added in the epilogue.
-    float csum[NPA][8];
-    float csum_t[8];
+    // weights the PV product multiplies V with); each read is conflict-free.
+    //  64-column atoms: csum[a][j] is column 64a + 8(L%8) + j, summed over the
+    //    warp's token rows L/8 + 4k (k < 8);
+    //  16-column atoms: csum[m][j] is column 16(L/8 + 4m) + 8(L%2) + j, summed
+    //    over rows (L%8)/2 + 4k (k < 8) (a quarter warp reads four rows of one atom).
+    // The lanes and the four warps are added in the epilogue.
+    float csum[NCS][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      csum_t[j] = 0.f;
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int a = 0; a < NPA; ++a) csum[a][j] = 0.f;
-    }
-    const int cs_chunk = lane & 7;
+      for (int a = 0; a < NCS; ++a) csum[a][j] = 0.f;
+    auto csum_col = [&](int a) -> int {   // first column of csum[a] for this lane (>= NQ: none)
+      return SW32 ? 16 * ((lane >> 3) + 4 * a) + 8 * (lane & 1) : 64 * a + 8 * (lane & 7);
+    };
     // Draft CTA: the tree masks.  Node `row` walks its root path (its ancestor
     // set), then, after the group barrier, gathers its descendant set: bit n
     // set when node n has `row` on its root path (itself included).
@@ -674,15 +693,14 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // rescale what O^T and the column sums hold to the new maxima: this
         // thread's dim (both halves) across every query column
 #pragma unroll
-        for (int a = 0; a < NPA; ++a) {
-          const float4 f0 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[0];
-          const float4 f1 = reinterpret_cast<const float4*>(sm->alpha + a * 64 + cs_chunk * 8)[1];
-          csum[a][0] *= f0.x; csum[a][1] *= f0.y; csum[a][2] *= f0.z; csum[a][3] *= f0.w;
-          csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
-        }
-        if (TAIL) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) csum_t[j] *= sm->alpha[128 + 8 * (lane & 1) + j];
+        for (int a = 0; a < NCS; ++a) {
+          const int c0 = csum_col(a);
+          if (c0 < NQ) {
+            const float4 f0 = reinterpret_cast<const float4*>(sm->alpha + c0)[0];
+            const float4 f1 = reinterpret_cast<const float4*>(sm->alpha + c0)[1];
+            csum[a][0] *= f0.x; csum[a][1] *= f0.y; csum[a][2] *= f0.z; csum[a][3] *= f0.w;
+            csum[a][4] *= f1.x; csum[a][5] *= f1.y; csum[a][6] *= f1.z; csum[a][7] *= f1.w;
+          }
         }
 #pragma unroll 1
         for (int mb = 0; mb < 2; ++mb) {
@@ -716,16 +734,13 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       } else if (i > 0) {
         if (!mbar_spin(bar(CSUM_B), (uint32_t)(i - 1) & 1u, &sm->abort, p.dev_status)) break;
       }
-      // P^T row of this token: 64-column atoms, then the tail
+      // P^T row of this token, 16 bytes (8 columns) at a time
 #pragma unroll
       for (int ch = 0; ch < NQ / 8; ++ch) {
         const uint4 w = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        if (ch < NQA / 8) {
-          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kPAtomB + p_off(hr, ch & 7)) = w;
-        } else {
-          const int tc = ch - NQA / 8;   // 0 or 1
-          *reinterpret_cast<uint4*>(sPt + hr * 32 + ((tc ^ ((hr >> 2) & 1)) << 4)) = w;
-        }
+        const uint32_t off = SW32 ? (uint32_t)((ch >> 1) * kPAtomB + hr * 32 + (((ch & 1) ^ ((hr >> 2) & 1)) << 4))
+                                  : (uint32_t)((ch >> 3) * kPAtomB) + p_off(hr, ch & 7);
+        *reinterpret_cast<uint4*>(sP + off) = w;
       }
       tc_fence_before();
       fence_async_smem();
@@ -734,12 +749,19 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       // Column sums of this tile's P from the rows this warp just wrote (the
       // same bf16 weights the PV product multiplies V with), while PV runs.
 #pragma unroll
-      for (int a = 0; a < NPA; ++a) {
-        if (a * 64 + cs_chunk * 8 < NQA) {
+      for (int a = 0; a < NCS; ++a) {
+        if (csum_col(a) < NQ) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int r = (quarter & 1) * 32 + (lane >> 3) + 4 * k;
-            const uint4 pv = *reinterpret_cast<const uint4*>(sP + a * kPAtomB + p_off(r, cs_chunk));
+            uint32_t off;
+            if (SW32) {
+              const int r = (quarter & 1) * 32 + ((lane & 7) >> 1) + 4 * k;
+              off = (uint32_t)(((lane >> 3) + 4 * a) * kPAtomB + r * 32 + (((lane & 1) ^ ((r >> 2) & 1)) << 4));
+            } else {
+              const int r = (quarter & 1) * 32 + (lane >> 3) + 4 * k;
+              off = (uint32_t)(a * kPAtomB) + p_off(r, lane & 7);
+            }
+            const uint4 pv = *reinterpret_cast<const uint4*>(sP + off);
             const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -747,20 +769,6 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
               csum[a][2 * e] += f.x;
               csum[a][2 * e + 1] += f.y;
             }
-          }
-        }
-      }
-      if (TAIL) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int r = (quarter & 1) * 32 + (lane >> 1) + 16 * k;
-          const uint4 pv = *reinterpret_cast<const uint4*>(sPt + r * 32 + (((lane & 1) ^ ((r >> 2) & 1)) << 4));
-          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
-            csum_t[2 * e] += f.x;
-            csum_t[2 * e + 1] += f.y;
           }
         }
       }
@@ -776,39 +784,27 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // two dims of one output row (64 bytes per row per store instruction).
     bool ok_epi = !*(volatile int*)&sm->abort;
     if (ok_epi) {
+      // lanes holding the same columns: L/8 for 64-column atoms, (L%8)/2 for 16-column atoms
 #pragma unroll
-      for (int a = 0; a < NPA; ++a)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 8);
-          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], 16);
-        }
-      if (TAIL) {
+      for (int a = 0; a < NCS; ++a)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 2);
-          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 4);
-          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 8);
-          csum_t[j] += __shfl_xor_sync(0xffffffffu, csum_t[j], 16);
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], SW32 ? 2 : 8);
+          csum[a][j] += __shfl_xor_sync(0xffffffffu, csum[a][j], SW32 ? 4 : 16);
         }
-      }
       // red[] may still be read by another warp's last max reduction: barrier first
       ok_epi = group_sync();
       if (ok_epi) {
-        if (lane < 8) {
+        if (SW32 ? (lane & 6) == 0 : lane < 8) {
 #pragma unroll
-          for (int a = 0; a < NPA; ++a) {
-            if (a * 64 + lane * 8 < NQA) {
-              float4* dst = reinterpret_cast<float4*>(&sm->red[sw][a * 64 + lane * 8]);
+          for (int a = 0; a < NCS; ++a) {
+            const int c0 = csum_col(a);
+            if (c0 < NQ) {
+              float4* dst = reinterpret_cast<float4*>(&sm->red[sw][c0]);
               dst[0] = make_float4(csum[a][0], csum[a][1], csum[a][2], csum[a][3]);
               dst[1] = make_float4(csum[a][4], csum[a][5], csum[a][6], csum[a][7]);
             }
           }
-        }
-        if (TAIL && lane < 2) {
-          float4* dst = reinterpret_cast<float4*>(&sm->red[sw][128 + lane * 8]);
-          dst[0] = make_float4(csum_t[0], csum_t[1], csum_t[2], csum_t[3]);
-          dst[1] = make_float4(csum_t[4], csum_t[5], csum_t[6], csum_t[7]);
         }
         ok_epi = group_sync();
       }
