@@ -643,14 +643,56 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       };
       // Fast pass (every tile after the first): P with the running maxima,
       // and whether any score exceeds its column's maximum by more than 2^8.
+      // A context tile outside a window's band has no per-element mask (a
+      // token row is visible to every column or to none), so its scores go
+      // straight from tensor memory into exp2(s * scale - m), 64 columns per
+      // tensor-memory wait.
       bool slow = true;
+      const bool plain = !has_draft && !(W > 0 && t0 < L - W + 1 + kMaxNodes);
       if (i > 0) {
         float dmax = -INFINITY;
+        if (plain) {
+          constexpr int NC = NQ / 16;   // 16-column chunks
 #pragma unroll
-        for (int g32 = 0; g32 < NG; ++g32) {
-          float v[32];
-          load_scores(g32, v);
-          dmax = fmaxf(dmax, make_p(g32, v));
+          for (int c0 = 0; c0 < NC; c0 += 4) {
+            float a[4][16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (c0 + c < NC) tmem_ld16(s_addr + (c0 + c) * 16, a[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (c0 + c < NC) {
+                const int col = (c0 + c) * 16;
+                float mm[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float4 m4 = reinterpret_cast<const float4*>(sm->m + col)[k];
+                  mm[4 * k] = m4.x; mm[4 * k + 1] = m4.y; mm[4 * k + 2] = m4.z; mm[4 * k + 3] = m4.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const float d0 = fmaf(a[c][e], kScaleLog2, -mm[e]);
+                  const float d1 = fmaf(a[c][e + 1], kScaleLog2, -mm[e + 1]);
+                  dmax = fmaxf(dmax, fmaxf(d0, d1));
+                  const __nv_bfloat162 h = __floats2bfloat162_rn(fast_exp2(d0), fast_exp2(d1));
+                  pk[(col + e) / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+              }
+            }
+          }
+          if (row >= valid) {   // past the context: no weight (whatever the stale scores were)
+#pragma unroll
+            for (int k = 0; k < NQ / 2; ++k) pk[k] = 0u;
+            dmax = -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int g32 = 0; g32 < NG; ++g32) {
+            float v[32];
+            load_scores(g32, v);
+            dmax = fmaxf(dmax, make_p(g32, v));
+          }
         }
         if (lane == 0) sm->flag[i & 1][sw] = 0;
         __syncwarp();
