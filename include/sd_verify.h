@@ -185,16 +185,23 @@ sd_status sd_verify_attn_fp8(const sd_shape* shape, const void* q, const void* k
  * synchronisation it may cause) is not allowed.  This entry point takes the
  * same inputs and outputs as sd_verify_attn but no workspace: the split
  * partials go to a scratch array of SD_NOALLOC_SCRATCH_BYTES that the library
- * keeps in device memory (every GPU that loads the library holds it until the
- * process exits).  It allocates nothing and calls no allocating routine.
+ * keeps in device memory.  It calls no allocating routine.
  *
- *  - The first call on each device looks up the array's address on that
- *    device (with it current) and caches it; make that first call before any
- *    stream capture.
- *  - Every call shares the one array and it keeps the last call's contents
- *    (nothing in it needs to start at zero).  Calls that may overlap on the GPU
- *    — on unordered streams or from several threads — race on it.
- *  - A shape whose scratch need (sd_verify_attn_workspace_size) exceeds
+ *  - The array is device memory of the library's module, which the CUDA
+ *    runtime loads lazily: the first call on a device loads it and reserves
+ *    the array then (and can fail with SD_ERR_CUDA when the device has no
+ *    room); the device keeps it until the process exits.  Later calls
+ *    allocate nothing.  Make the first call early and before any stream
+ *    capture.
+ *  - The first call in a CUDA context (normally the device's primary context,
+ *    i.e. once per device) looks up the array's address with that context
+ *    current and keeps it under the context's unique id; another context, or
+ *    the new context after a device reset, does its own lookup.
+ *  - Every call in a context shares the one array and it keeps the last call's
+ *    contents (nothing in it needs to start at zero).  Calls that may overlap
+ *    on the GPU — on unordered streams or from several threads — race on it.
+ *  - A shape that sd_verify_attn would reject returns the same status; a shape
+ *    whose scratch need (sd_verify_attn_workspace_size) exceeds
  *    SD_NOALLOC_SCRATCH_BYTES is rejected with SD_ERR_WORKSPACE before any
  *    launch.  Other arguments and errors are as for sd_verify_attn.
  */

@@ -233,6 +233,11 @@ sd_status kv_commit(const sd_shape* shape, int num_layers, void* const* k_cache_
 
 }  // namespace
 
+sd_status sdv::verify_shape_status(const sd_shape* s) {
+  BatchDesc bd;
+  return check_shape(s, &bd);
+}
+
 extern "C" {
 
 const char* sd_status_string(sd_status s) {

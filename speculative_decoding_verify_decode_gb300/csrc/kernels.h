@@ -26,6 +26,9 @@ TcPlan tc_plan(int max_nodes);
 size_t tc_smem_bytes(int nq);
 cudaError_t launch_attn_tc8(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 
+// Host-side validation of a verify-attention shape (the status sd_verify_attn returns for it).
+sd_status verify_shape_status(const sd_shape* s);
+
 // Log-sum-exp merge of the split partials into the bf16 output.
 cudaError_t launch_attn_merge(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 

@@ -57,3 +57,18 @@ def test_with_ctx_stable_sets_only_the_flag():
     assert list(stable.indptr) == list(base.indptr)
     assert base.c.ctx_stable == 0 and stable.c.ctx_stable == 1
     assert stable.with_ctx_stable(False).c.ctx_stable == 0
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a C compiler")
+def test_header_constants_match_the_binding(tmp_path):
+    """Constants the binding copies from sd_verify.h, as a C compiler evaluates them."""
+    consts = {"SD_NOALLOC_SCRATCH_BYTES": native.NOALLOC_SCRATCH_BYTES, "SD_MAX_NODES": native.MAX_NODES,
+              "SD_MAX_BATCH": native.MAX_BATCH, "SD_MAX_LAYERS": native.MAX_LAYERS,
+              "SD_DEV_TIMEOUT": native.SD_DEV_TIMEOUT, "SD_DEV_BAD_PAGE": native.SD_DEV_BAD_PAGE}
+    prints = " ".join(f'printf(" %llu", (unsigned long long)({k}));' for k in consts)
+    src = tmp_path / "consts.c"
+    src.write_text(f'#include <stdio.h>\n#include "sd_verify.h"\nint main(void) {{ {prints} printf("\\n"); return 0; }}\n')
+    exe = tmp_path / "consts"
+    subprocess.run(["gcc", "-std=c11", "-I", INC, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got == list(consts.values())

@@ -23,6 +23,15 @@ def _attn_args(w, layer=0):
             d["ctx_lens"], d["parents"])
 
 
+def test_invalid_shape_returns_the_shape_status():
+    ensure_built()
+    shape = native.Shape(np.array([0, 9]), 64, 64)
+    shape.c.head_dim = 128                       # geometry the library does not support
+    with pytest.raises(native.SdError) as e:
+        native.sd_verify_attn_noalloc(shape, 16, 16, 16, 16, 16, 16, 16, 16, 16, stream=0)   # never dereferenced
+    assert e.value.status == native.SD_ERR_UNSUPPORTED
+
+
 def test_oversized_shape_is_rejected_before_any_launch():
     ensure_built()
     # 4 sequences of 64 nodes cut into 64 splits each need far more than the fixed scratch
@@ -55,3 +64,26 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
         err = float(np.abs(f64(out) - ref).max())
         assert err <= tight_bound(ref), err
         assert float(np.abs(f64(lse) - f64(st.lse[0])).max()) <= 1e-5
+
+
+@pytest.mark.gpu
+def test_calls_after_the_first_leave_free_device_memory_unchanged():
+    """The first call in a context may load the library's module (and with it the scratch array);
+    every later call allocates nothing: free device memory stays the same, byte for byte."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    ensure_built()
+    w = synth.make_workload("ddtree22_ctx32k", device="cuda", layers=1, logits=False)
+    st = VerifyStep(w.q_indptr, w.max_pages, w.num_pool_pages, 1, 16)
+    args = _attn_args(w, 0)
+    out = torch.empty_like(st.out[0])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    native.sd_verify_attn_noalloc(st.shape, *args, out, None, status)   # warm-up: may load the module
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        native.sd_verify_attn_noalloc(st.shape, *args, out, None, status)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert int(status.item()) == 0
