@@ -641,15 +641,37 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         return dm;
       };
-      // Fast pass (every tile after the first): P with the running maxima,
-      // and whether any score exceeds its column's maximum by more than 2^8.
-      // A context tile outside a window's band has no per-element mask (a
-      // token row is visible to every column or to none), so its scores go
-      // straight from tensor memory into exp2(s * scale - m), 64 columns per
-      // tensor-memory wait.
+      // Fast pass (every tile after the first, and the first one of a plain
+      // context split): P with the running maxima, and whether any score
+      // exceeds its column's maximum by more than 2^8.  A context tile outside
+      // a window's band has no per-element mask (a token row is visible to
+      // every column or to none), so its scores go straight from tensor memory
+      // into exp2(s * scale - m), 64 columns per tensor-memory wait.
       bool slow = true;
       const bool plain = !has_draft && !(W > 0 && t0 < L - W + 1 + kMaxNodes);
-      if (i > 0) {
+      if (i == 0 && plain) {
+        // The running maxima start at token row 0's scores (every column sees
+        // that token).  Any score more than 2^8 above them takes the exact
+        // path below, as in a later tile, so this only saves the three-pass
+        // maximum search of the first tile in the common case.
+        if (quarter == 0) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < NQ / 16; ++c0) {
+            float a[16];
+            tmem_ld16(s_addr + c0 * 16, a);
+            tmem_wait_ld();
+            if (lane == 0) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                reinterpret_cast<float4*>(sm->m + c0 * 16)[k] =
+                    make_float4(a[4 * k] * kScaleLog2, a[4 * k + 1] * kScaleLog2, a[4 * k + 2] * kScaleLog2,
+                                a[4 * k + 3] * kScaleLog2);
+            }
+          }
+        }
+        if (!group_sync()) break;
+      }
+      if (i > 0 || plain) {
         float dmax = -INFINITY;
         if (plain) {
           constexpr int NC = NQ / 16;   // 16-column chunks
