@@ -97,8 +97,9 @@ struct Ring {
   static constexpr int kFixed = kQB + kPB + (int)sizeof(RSmall<kCols>);
   static constexpr int kBudget = kSmemMax - kFixed - kKTileB;
   static constexpr int RV0 = kBudget / kPageB;
-  static constexpr int RV = RV0 > 12 ? 12 : RV0;          // V slots, one page each
-  static constexpr int kNumBars = 2 * RV + 12;
+  static constexpr int RV = RV0 >= 12 ? 12 : RV0 / 4 * 4;   // V pages: ring slots of four pages (half a tile)
+  static constexpr int RVH = RV / 4;
+  static constexpr int kNumBars = 2 * RVH + 12;
   static constexpr size_t kSmem = (size_t)kQB + (size_t)kKTileB + (size_t)RV * kPageB + kPB + sizeof(RSmall<kCols>);
   static_assert(RV >= 8, "the V ring holds at least a whole tile");
   static_assert(kNumBars <= kMaxBars, "barrier array too small");
@@ -113,16 +114,17 @@ __global__ void __launch_bounds__(kRingThreads, 1)
 attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const AttnParams p, const BatchDesc bd, const int hpc, const int hparts) {
   using R = Ring<NQ>;
-  constexpr int NG = R::NG, RV = R::RV;
+  constexpr int NG = R::NG, RV = R::RV, RVH = R::RVH;
+  constexpr int kHalfB = 4 * kPageB;   // one V ring slot: four pages
   constexpr bool SW32 = R::kSW32;
   constexpr int kPAtomB = R::kPAtom;
   // column sums: 64-column atoms (a lane: 8 columns of each), or 16-column atoms (a lane: up to three)
   constexpr int NCS = SW32 ? 3 : R::kPA;
   constexpr uint32_t kColS = 0, kColO = NQ;   // tensor-memory columns: S^T, then O^T (two halves of NQ)
-  // Barriers: V slot full / empty, then the tile-level ones.  CSUM_A / CSUM_B:
+  // Barriers: V half-slot full / empty, then the tile-level ones.  CSUM_A / CSUM_B:
   // the warps of a half tile have read their P^T rows back (column sums).
-  constexpr int B_VF = 0, B_VE = RV;
-  constexpr int K_FULL = 2 * RV, K_EMPTY = K_FULL + 1, S_FULL = K_FULL + 2, S_FREE = K_FULL + 3,
+  constexpr int B_VF = 0, B_VE = RVH;
+  constexpr int K_FULL = 2 * RVH, K_EMPTY = K_FULL + 1, S_FULL = K_FULL + 2, S_FREE = K_FULL + 3,
                 P_FULL_A = K_FULL + 4, O_HALF = K_FULL + 5, P_FULL_B = K_FULL + 6, O_DONE = K_FULL + 7,
                 CSUM_A = K_FULL + 8, CSUM_B = K_FULL + 9, GROUP = K_FULL + 10;
   // No static shared memory: the dynamic window starts on a 1024-byte boundary
@@ -299,7 +301,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int n_ctx = has_draft ? 0 : n_tiles;
     const __nv_bfloat16* cache = is_k ? p.k_cache : p.v_cache;
     int page_next = page0;   // lane l < 8: page id of page l of the coming tile, fetched a tile ahead
-    int fills = 0;           // K tiles, or V pages, issued so far (V page f goes to ring slot f % RV)
+    int fills = 0;           // K tiles, or V half tiles, issued so far (V half f goes to ring slot f % RVH)
     bool ok = true;
     for (int i = 0; i < n_ctx && ok; ++i) {
       const int t0 = ctx_begin + i * kT;
@@ -337,45 +339,43 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           tma_load_page(smem_u32(sK + lane * kPageB), &tm_k, (page * kHkv + g) * 2, bar(K_FULL));
         ++fills;
       } else {
-        // V: the tile's pages up to the last valid token, one ring slot each,
-        // in two groups of four (pages 0-3 free up as PV consumes the previous
-        // tile's first half, pages 4-7 with its second half).  Lane j waits for
-        // the slot of page j; then the group's lanes issue their boxes
-        // together, as one warp instruction: boxes issued one thread after
-        // another cannot keep enough bytes in flight.  A page goes by TMA when
-        // it is in range and all its 16 tokens are valid; otherwise the warp
-        // copies it with plain loads, zero past the context (P is 0 there, but
-        // 0 times stale data could be NaN).
+        // V: the tile's pages up to the last valid token, in two halves of up
+        // to four pages (0-3, 4-7).  A half takes one ring slot of four pages
+        // with one full and one empty barrier: it is issued once PV has
+        // consumed the slot's previous half, and PV waits for it once.  A page
+        // goes by TMA when it is in range and all its 16 tokens are valid
+        // (the half's lanes issue their boxes together, as one warp
+        // instruction); otherwise the warp copies it with plain loads first,
+        // zero past the context (P is 0 there, but 0 times stale data could be
+        // NaN).
         const int npg = (valid + kPage - 1) / kPage;
-        const int myslot = (fills + lane) % RV;
-        const uint32_t myph = (uint32_t)((fills + lane) / RV) & 1u;
         const bool full = lane < npg && page >= 0 && (lane + 1) * kPage <= valid;
         for (int grp = 0; grp < 2 && grp * 4 < npg && ok; ++grp) {
-          const bool mine = lane >= 4 * grp && lane < 4 * grp + 4 && lane < npg;
-          bool lane_ok = true;
-          if (mine) lane_ok = mbar_wait(bar(B_VE + myslot), myph ^ 1u, &sm->abort, p.dev_status);
-          ok = __all_sync(0xffffffffu, lane_ok);
+          const int hs = fills % RVH;
+          if (lane == 0) ok = mbar_wait(bar(B_VE + hs), ((uint32_t)(fills / RVH) & 1u) ^ 1u, &sm->abort, p.dev_status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          if (mine && full) {
-            mbar_expect_tx(bar(B_VF + myslot), (uint32_t)kPageB);
-            tma_load_page(smem_u32(sV + myslot * kPageB), &tm_v, (page * kHkv + g) * 2, bar(B_VF + myslot));
+          uint8_t* slot = sV + hs * kHalfB;
+          const bool mine = lane >= 4 * grp && lane < 4 * grp + 4 && lane < npg;
+          for (uint32_t part = __ballot_sync(0xffffffffu, mine && !full); part != 0u; part &= part - 1u) {
+            const int j = __ffs(part) - 1;
+            const int pg = __shfl_sync(0xffffffffu, page, j);
+            stage_rows(slot + (j - 4 * grp) * kPageB, 0, kPage, [&](int r) -> const __nv_bfloat16* {
+              return (pg >= 0 && j * kPage + r < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + r) * kDim
+                                                        : nullptr;
+            }, lane, 32);
           }
+          fence_async_smem();
+          const uint32_t tma_n = (uint32_t)__popc(__ballot_sync(0xffffffffu, mine && full));
           __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_VF + hs), tma_n * (uint32_t)kPageB);   // the half's one arrival
+          __syncwarp();
+          if (mine && full)
+            tma_load_page(smem_u32(slot + (lane - 4 * grp) * kPageB), &tm_v, (page * kHkv + g) * 2, bar(B_VF + hs));
+          __syncwarp();
+          ++fills;
         }
         if (!ok) break;
-        for (uint32_t part = __ballot_sync(0xffffffffu, lane < npg && !full); part != 0u; part &= part - 1u) {
-          const int j = __ffs(part) - 1;
-          const int pg = __shfl_sync(0xffffffffu, page, j);
-          const int sj = (fills + j) % RV;
-          stage_rows(sV + sj * kPageB, 0, kPage, [&](int r) -> const __nv_bfloat16* {
-            return (pg >= 0 && j * kPage + r < valid) ? cache + (((size_t)pg * kHkv + g) * kPage + r) * kDim
-                                                      : nullptr;
-          }, lane, 32);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_VF + sj));
-        }
-        fills += npg;
       }
       // early context loads: the later slots free up only as the compute warps (which wait) progress
       if (early && i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -384,7 +384,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // After an abort no copy may still be landing when the CTA ends: wait,
     // bounded, for the last fill of every slot.
     if (lane == 0 && *(volatile int*)&sm->abort) {
-      const int nslots = is_k ? 1 : RV;
+      const int nslots = is_k ? 1 : RVH;
       for (int j = 0; j < nslots && j < fills; ++j) {
         const int last = j + (fills - 1 - j) / nslots * nslots;   // the last fill of slot j
         const uint32_t parity = (uint32_t)(last / nslots) & 1u;
@@ -461,12 +461,13 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   } else if (warp == kRWarpPV) {
     // ------------------------------------------------------------ PV issuer
     // PV of tile i, one page (16 tokens) at a time, in two halves: pages 0-3
-    // once P^T holds token rows 0-63 (P_FULL_A), then pages 4-7 once the
-    // softmax has replaced them by rows 64-127 (P_FULL_B).
+    // once P^T holds token rows 0-63 (P_FULL_A) and the half's V slot has
+    // landed, then pages 4-7 once the softmax has replaced them by rows 64-127
+    // (P_FULL_B).
     if (lane == 0) {
       constexpr uint32_t kIdPV = f16_idesc(128, NQ, 1, 1);
       const uint32_t v_addr = smem_u32(sV), p_addr = smem_u32(sP);
-      int fills = 0;   // V pages consumed so far (page f in ring slot f % RV)
+      int fills = 0;   // V halves consumed so far (half f in ring slot f % RVH)
       bool ok = true;
       for (int i = 0; i < n_tiles && ok; ++i) {
         const int npg = (tile_valid(i) + kPage - 1) / kPage;
@@ -474,16 +475,15 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           ok = mbar_wait(bar(half ? P_FULL_B : P_FULL_A), (uint32_t)i & 1u, &sm->abort, p.dev_status);
           if (!ok) break;
           const int nh = min(4, npg - 4 * half);   // pages of this half (none: an empty second half)
+          const int hs = fills % RVH;
+          if (nh > 0 && !has_draft) {
+            ok = mbar_wait(bar(B_VF + hs), (uint32_t)(fills / RVH) & 1u, &sm->abort, p.dev_status);
+            if (!ok) break;
+          }
           tc_fence_after();
-          for (int jj = 0; jj < nh && ok; ++jj) {
-            // each page as soon as it has landed
-            const int slot = has_draft ? 4 * half + jj : fills % RV;
-            if (!has_draft) {
-              ok = mbar_wait(bar(B_VF + slot), (uint32_t)(fills / RV) & 1u, &sm->abort, p.dev_status);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            const uint32_t va = v_addr + (uint32_t)slot * kPageB;
+          for (int jj = 0; jj < nh; ++jj) {
+            const uint32_t va = has_draft ? v_addr + (uint32_t)(4 * half + jj) * kPageB
+                                          : v_addr + (uint32_t)hs * kHalfB + (uint32_t)jj * kPageB;
             const uint32_t acc = (i > 0 || half > 0 || jj > 0) ? 1u : 0u;
             const uint32_t prow = (uint32_t)jj * 16;   // the page's first row in the half tile
 #pragma unroll
@@ -495,10 +495,10 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                                        : sw128_desc(p_addr + prow * 128, kPAtomB, 1024);
               umma(tmem + kColO + mb * NQ, a, bd, kIdPV, acc);
             }
-            if (!has_draft) {
-              umma_commit(bar(B_VE + slot));
-              ++fills;
-            }
+          }
+          if (nh > 0 && !has_draft) {
+            umma_commit(bar(B_VE + hs));
+            ++fills;
           }
           if (!ok) break;
           umma_commit(bar(half ? O_DONE : O_HALF));
