@@ -20,18 +20,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// One 128-thread block per (node row, query head): four warps each take every
-// fourth split, lane t owning dims 8t..8t+7 (16 bytes of each partial row).  A
+// One 256-thread block per (node row, query head): eight warps each take every
+// eighth split, lane t owning dims 8t..8t+7 (16 bytes of each partial row).  A
 // thread issues the loads of up to kBatch of its splits before it uses any
-// (one round of memory latency for up to 4 * kBatch splits) and keeps its
-// warp's running (max, sum, weighted sum) in base 2; the four warps are
-// combined once, through shared memory.  The blocks are scheduled while the
-// split kernel runs (one warp per scheduler, a few registers each), so several
-// fit beside a resident split CTA and none keeps the next layer's split CTAs
-// off an SM once the current one exits.
-constexpr int kMergeThreads = 128;
+// (one round of memory latency for up to 8 * kBatch = 40 splits) and keeps its
+// warp's running (max, sum, weighted sum) in base 2; the eight warps are
+// combined once, through shared memory.  The blocks are launched while the
+// split kernel runs and become resident as its CTAs exit.
+constexpr int kMergeThreads = 256;
 constexpr int kMergeGroups = kMergeThreads / 32;
-constexpr int kBatch = 9;
+constexpr int kBatch = 5;
 
 __device__ __forceinline__ void add_weighted(float (&acc)[8], float wk, const uint4& o) {
   const float2 a = unpack_bf16(o.x), b = unpack_bf16(o.y), c = unpack_bf16(o.z), d = unpack_bf16(o.w);
