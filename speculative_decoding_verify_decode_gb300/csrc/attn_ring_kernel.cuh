@@ -319,8 +319,10 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // K: the whole tile, one 8 KB box per page.  Pages past the context are
         // not loaded (their rows are masked); pages with an id out of range
         // are zeros.
-        if (lane == 0) ok = mbar_wait(bar(K_EMPTY), (uint32_t)(i & 1) ^ 1u, &sm->abort, p.dev_status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        // every lane waits (a lone waiting lane while the rest of the warp sits
+        // at a warp-wide step resumed about 0.7 us after the phase completed)
+        ok = mbar_wait(bar(K_EMPTY), (uint32_t)(i & 1) ^ 1u, &sm->abort, p.dev_status);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint32_t tma_mask = __ballot_sync(0xffffffffu, lane < 8 && page >= 0);
         const uint32_t zero_mask = __ballot_sync(0xffffffffu, bad);
@@ -352,8 +354,8 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const bool full = lane < npg && page >= 0 && (lane + 1) * kPage <= valid;
         for (int grp = 0; grp < 2 && grp * 4 < npg && ok; ++grp) {
           const int hs = fills % RVH;
-          if (lane == 0) ok = mbar_wait(bar(B_VE + hs), ((uint32_t)(fills / RVH) & 1u) ^ 1u, &sm->abort, p.dev_status);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          ok = mbar_wait(bar(B_VE + hs), ((uint32_t)(fills / RVH) & 1u) ^ 1u, &sm->abort, p.dev_status);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           uint8_t* slot = sV + hs * kHalfB;
           const bool mine = lane >= 4 * grp && lane < 4 * grp + 4 && lane < npg;
