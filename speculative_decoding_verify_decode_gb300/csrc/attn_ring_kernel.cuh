@@ -237,7 +237,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   // t): Q^T (K-major, block-major; column q = node * hpc + head-in-part, zeros
   // past `rows`) and, in the draft CTA, the draft block: K rows into the K tile
   // and V rows into the first V slots (both group-major; node t = token row t).  A row table (source, destination, block
-  // stride) is built first, then one pass of 16-byte copies with up to 16
+  // stride) is built first, then one pass of 16-byte copies with up to 12
   // loads in flight per thread; the last round repeats the final chunk instead
   // of branching, so the unrolled copies stay independent.
   auto stage_operands = [&](const int t, const int nthr, const bool all_warps) {
@@ -264,7 +264,7 @@ attn_ring_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     if (all_warps) __syncthreads();
     else asm volatile("bar.sync 3, 192;" ::: "memory");   // the compute warps
-    constexpr int U = 16;
+    constexpr int U = 12;
     const int tasks = n_stage * 32;
     for (int t0 = t; t0 - t < tasks; t0 += nthr * U) {
       uint4 v[U];
