@@ -460,10 +460,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           if (early && uses == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
           const uint32_t slot_full = bar(is_k ? K8_FULL0 + h : V8_FULL0 + h);
           const uint32_t buf_empty = bar(is_k ? K_EMPTY : V_EMPTY0);
-          if (lane == 0)
-            ok = mbar_wait(slot_full, (uint32_t)(i & 1), &sm->abort, p.dev_status) &&
-                 mbar_wait(buf_empty, (uint32_t)(uses & 1) ^ 1u, &sm->abort, p.dev_status);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          // every lane waits (a lone waiting lane while the rest of the warp sits at a
+          // warp-wide step resumes late)
+          ok = mbar_wait(slot_full, (uint32_t)(i & 1), &sm->abort, p.dev_status) &&
+               mbar_wait(buf_empty, (uint32_t)(uses & 1) ^ 1u, &sm->abort, p.dev_status);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const uint32_t src_base = smem_u32((is_k ? sK8 : sV8) + h * kSlotB) + src0;
           // rows of this lane that hold codes (all of them for a whole tile)
