@@ -36,9 +36,11 @@ from speculative_decoding_verify_decode_gb300.step import VerifyStep, device_inp
 METRIC = "verify steps/s"
 DEFAULT_CONFIG = "ddtree22_ctx128k"
 EXTRA_CONFIGS = ["tiny_chain_ctx512", "chain8_ctx4k", "ddtree22_ctx32k", "conc8_chain4_ragged"]
-ATTN_SRCS = [os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc", f)
-             for f in ("attn_ring_kernel.cuh", "attn_ring_launch.cuh", "attn_ring.cu", "tc_ptx.cuh",
-                       "attn_tc_kernel.cuh", "attn_tc8.cu")]
+CSRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc")
+# the sources of each attention kernel: a traffic figure holds while they are unchanged
+ATTN_SRCS = {"bf16": [os.path.join(CSRC, f) for f in ("attn_ring_kernel.cuh", "attn_ring_launch.cuh",
+                                                      "attn_ring.cu", "attn_ring_win.cu", "tc_ptx.cuh")],
+             "fp8": [os.path.join(CSRC, f) for f in ("attn_tc_kernel.cuh", "attn_tc8.cu", "tc_ptx.cuh")]}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
 
 
@@ -69,22 +71,22 @@ def attn_bytes_per_layer(w) -> int:
     return ctx * per_token + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
 
 
-def kernel_sha() -> str:
+def kernel_sha(kv: str) -> str:
     h = hashlib.sha256()
-    for src in ATTN_SRCS:
+    for src in ATTN_SRCS[kv]:
         with open(src, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
 
-def traffic_for(config: str):
-    """dram bytes per attention launch from the last ncu capture, if the kernel is unchanged."""
+def traffic_for(config: str, kv: str):
+    """dram bytes per attention launch from the last ncu capture, if that kernel's sources are unchanged."""
     try:
         with open(TRAFFIC_FILE) as f:
             for line in f:
                 parts = line.split()
                 if len(parts) >= 3 and not line.startswith("#") and parts[0] == config:
-                    return float(parts[2]) if parts[1] == kernel_sha() else None
+                    return float(parts[2]) if parts[1] == kernel_sha(kv) else None
     except OSError:
         pass
     return None
@@ -522,7 +524,7 @@ def run_ours(args, world, rank, local):
         "accepted_tok_per_s": world * m["accepted"] * 1000.0 / ms_per_step,
         "kv_read_gbs": m["achieved"],
         "roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": m["peak"], "unit": "GB/s",
-                     "frac": m["achieved"] / m["peak"], "traffic": traffic_for(args.config),
+                     "frac": m["achieved"] / m["peak"], "traffic": traffic_for(args.config, "fp8" if m["fp8"] else "bf16"),
                      "kernel": "verify attention of one layer (split kernel + merge), from a graph of all layers",
                      "alg_bytes_per_launch": m["alg"], "launch_ms": m["attn_ms"], "peak_kind": m["peak_kind"]},
         "e2e": {"value": world * 1000.0 / m["e2e_ms"], "unit": "steps/s", "h2d_bytes_per_step": m["h2d"],
