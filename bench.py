@@ -38,9 +38,10 @@ DEFAULT_CONFIG = "ddtree22_ctx128k"
 EXTRA_CONFIGS = ["tiny_chain_ctx512", "chain8_ctx4k", "ddtree22_ctx32k", "conc8_chain4_ragged"]
 CSRC = os.path.join(ROOT, "speculative_decoding_verify_decode_gb300", "csrc")
 # the sources of each attention kernel: a traffic figure holds while they are unchanged
-ATTN_SRCS = {"bf16": [os.path.join(CSRC, f) for f in ("attn_ring_kernel.cuh", "attn_ring_launch.cuh",
-                                                      "attn_ring.cu", "attn_ring_win.cu", "tc_ptx.cuh")],
-             "fp8": [os.path.join(CSRC, f) for f in ("attn_tc_kernel.cuh", "attn_tc8.cu", "tc_ptx.cuh")]}
+ATTN_SRCS = {"attn_ring_kernel": [os.path.join(CSRC, f) for f in ("attn_ring_kernel.cuh", "attn_ring_launch.cuh",
+                                                                  "attn_ring.cu", "attn_ring_win.cu", "tc_ptx.cuh")],
+             "attn_tc_kernel": [os.path.join(CSRC, f) for f in ("attn_tc_kernel.cuh", "attn_tc8.cu", "attn_tc16.cu",
+                                                                "tc_ptx.cuh")]}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.txt")
 
 
@@ -71,22 +72,24 @@ def attn_bytes_per_layer(w) -> int:
     return ctx * per_token + n * 24 * 512 * 2 + n * 4 * 512 * 2 + pages * 4
 
 
-def kernel_sha(kv: str) -> str:
+def kernel_sha(kernel: str) -> str:
     h = hashlib.sha256()
-    for src in ATTN_SRCS[kv]:
+    for src in ATTN_SRCS[kernel]:
         with open(src, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
 
-def traffic_for(config: str, kv: str):
-    """dram bytes per attention launch from the last ncu capture, if that kernel's sources are unchanged."""
+def traffic_for(config: str):
+    """dram bytes per attention launch from the last ncu capture of the workload, if the captured kernel's
+    sources (the kernel name ends each line) are unchanged."""
     try:
         with open(TRAFFIC_FILE) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) >= 3 and not line.startswith("#") and parts[0] == config:
-                    return float(parts[2]) if parts[1] == kernel_sha(kv) else None
+                if len(parts) >= 4 and not line.startswith("#") and parts[0] == config:
+                    kernel = parts[-1].split("<")[0]
+                    return float(parts[2]) if kernel in ATTN_SRCS and parts[1] == kernel_sha(kernel) else None
     except OSError:
         pass
     return None
@@ -524,7 +527,7 @@ def run_ours(args, world, rank, local):
         "accepted_tok_per_s": world * m["accepted"] * 1000.0 / ms_per_step,
         "kv_read_gbs": m["achieved"],
         "roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": m["peak"], "unit": "GB/s",
-                     "frac": m["achieved"] / m["peak"], "traffic": traffic_for(args.config, "fp8" if m["fp8"] else "bf16"),
+                     "frac": m["achieved"] / m["peak"], "traffic": traffic_for(args.config),
                      "kernel": "verify attention of one layer (split kernel + merge), from a graph of all layers",
                      "alg_bytes_per_launch": m["alg"], "launch_ms": m["attn_ms"], "peak_kind": m["peak_kind"]},
         "e2e": {"value": world * 1000.0 / m["e2e_ms"], "unit": "steps/s", "h2d_bytes_per_step": m["h2d"],

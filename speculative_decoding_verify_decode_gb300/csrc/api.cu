@@ -89,9 +89,17 @@ SplitPlan plan_splits(const sd_shape* s, const BatchDesc& bd, int hparts) {
   return SplitPlan{(int)chunk, (int)n};
 }
 
-// The plan of each cache kind: bf16 caches run the ring kernel, e4m3 caches the converter kernel.
+// The plan of each cache kind: bf16 caches run the ring kernel's plan, e4m3 caches the converter kernel's.
 SplitPlan plan_for(const sd_shape* s, const BatchDesc& bd, bool fp8) {
   return plan_splits(s, bd, fp8 ? tc_plan(bd.max_nodes).hparts : ring_plan(bd.max_nodes).hparts);
+}
+
+// bf16 caches: when every context split is a single tile and attn_tc_kernel cuts the query heads the
+// same way (so the grid, the plan and the workspace are the ring kernel's), the layer is a latency
+// chain and attn_tc_kernel's shorter one wins; otherwise the ring kernel streams the tiles.
+bool short_bf16(const SplitPlan& pl, const BatchDesc& bd) {
+  return pl.chunk == kTileTokens && tc_plan(bd.max_nodes).hparts == ring_plan(bd.max_nodes).hparts &&
+         tc_plan(bd.max_nodes).hpc * bd.max_nodes <= kTcMaxNQ;
 }
 
 size_t attn_workspace(const SplitPlan& pl, const BatchDesc& bd) {
@@ -181,7 +189,8 @@ sd_status verify_attn(const sd_shape* shape, const void* q, const void* k_cache,
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * kDim * sizeof(__nv_bfloat16)));
   }
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return cuda_status(fp8 ? launch_attn_tc8(p, bd, cs) : launch_attn_tc(p, bd, cs));
+  if (fp8) return cuda_status(launch_attn_tc8(p, bd, cs));
+  return cuda_status(short_bf16(pl, bd) ? launch_attn_tc16(p, bd, cs) : launch_attn_ring(p, bd, cs));
 }
 
 // sd_kv_commit and sd_kv_commit_fp8.

@@ -53,7 +53,7 @@ TcPlan ring_plan(int max_nodes) {
   return pl;
 }
 
-cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
+cudaError_t launch_attn_ring(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   CUtensorMap mk, mv;
   if (!ring_map(&mk, p.k_cache, p.num_pool_pages) || !ring_map(&mv, p.v_cache, p.num_pool_pages))
     return cudaErrorInvalidValue;

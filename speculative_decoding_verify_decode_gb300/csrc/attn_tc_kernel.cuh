@@ -1159,7 +1159,7 @@ cudaError_t launch_nq(const CUtensorMap& mk, const CUtensorMap& mv, const AttnPa
   return cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ, WIN, KV8>, mk, mv, p, bd, hpc, hparts);
 }
 
-// Dispatch over the compiled query-column widths (attn_tc.cu: bf16 caches, attn_tc8.cu: e4m3).
+// Dispatch over the compiled query-column widths (attn_tc16.cu: bf16 caches, attn_tc8.cu: e4m3).
 template <bool KV8>
 cudaError_t launch_tc_kind(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p, const BatchDesc& bd,
                            cudaStream_t st) {

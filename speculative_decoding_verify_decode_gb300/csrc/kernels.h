@@ -16,15 +16,18 @@ struct TcPlan {
 // bf16 caches: the ring-buffered kernel (attn_ring_kernel.cuh), up to 144 query columns per CTA.
 constexpr int kRingMaxNQ = 144;
 TcPlan ring_plan(int max_nodes);
-cudaError_t launch_attn_tc(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+cudaError_t launch_attn_ring(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 // its sliding-window instances (attn_ring_win.cu)
 cudaError_t launch_ring_window(const CUtensorMap& mk, const CUtensorMap& mv, const AttnParams& p,
                                const BatchDesc& bd, const TcPlan& pl, cudaStream_t st);
-// e4m3 caches (p.k_cache8 / p.v_cache8 with p.k_scale / p.v_scale): attn_tc_kernel.cuh, up to 96 columns.
+// attn_tc_kernel.cuh, up to 96 query columns per CTA: e4m3 caches (p.k_cache8 / p.v_cache8 with
+// p.k_scale / p.v_scale, attn_tc8.cu), and bf16 caches when every context split is a single tile
+// (attn_tc16.cu).
 constexpr int kTcMaxNQ = 96;
 TcPlan tc_plan(int max_nodes);
 size_t tc_smem_bytes(int nq);
 cudaError_t launch_attn_tc8(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
+cudaError_t launch_attn_tc16(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 
 // Host-side validation of a verify-attention shape (the status sd_verify_attn returns for it).
 sd_status verify_shape_status(const sd_shape* s);

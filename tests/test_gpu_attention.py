@@ -40,6 +40,10 @@ CASES = {
     "max_nodes64_ctx300": ([_tree(5, 63)], [300], 1.0, 2),
     "empty_context_tree": ([_tree(6, 22)], [0], 1.0, 0),
     "ctx_one_page_exact": ([synth.chain_parents(4), synth.chain_parents(4)], [16, 64], 0.5, 0),
+    # a chain over 4000 tokens: one tile per split (the automatic plan) runs attn_tc_kernel on bf16 caches,
+    # three tiles per split the ring kernel
+    "chain8_ctx4000_one_tile_splits": ([synth.chain_parents(8)], [4000], 1.0, 0),
+    "chain8_ctx4000_three_tile_splits": ([synth.chain_parents(8)], [4000], 1.0, 11),
 }
 
 
