@@ -150,14 +150,16 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t& lo, uin
 // memory: a 2 KB box of the 3-D code map at (x, 0, page * 4 + head).
 __device__ __forceinline__ void tma_load_k8(uint32_t dst, const CUtensorMap* map, int x, int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(0), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(0), "r"(z), "r"(bar), "l"(l2_evict_first())
       : "memory");
 }
-// `bytes` contiguous bytes (a multiple of 16, both addresses 16-byte aligned) into shared memory.
+// `bytes` contiguous bytes (a multiple of 16, both addresses 16-byte aligned) into shared memory, read
+// with the evict-first policy (context pages).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(l2_evict_first())
                : "memory");
 }
 // WIN: compiled with the sliding-window paths (band masks, depths); the

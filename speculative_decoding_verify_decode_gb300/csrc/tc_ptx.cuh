@@ -91,12 +91,22 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, int* ab
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// L2 policy for data read once (the context pages): its lines are the first
+// to be evicted, so streaming the cache does not push the kernels' code, the
+// page tables, the queries and the split partials out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // One page of one KV head (8 KB) into shared memory: the 4-D box of the
-// cache map at outer coordinate w, x = y = z = 0.
+// cache map at outer coordinate w, x = y = z = 0, read with the evict-first policy.
 __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int w, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %2, %2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar), "l"(l2_evict_first())
       : "memory");
 }
 
