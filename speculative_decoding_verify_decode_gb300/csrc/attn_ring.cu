@@ -20,13 +20,15 @@ PFN_cuTensorMapEncodeTiled_v12000 ring_encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // The cache viewed as 4-D: x = dim within a 64-dim block (contiguous),
 // y = slot within an 8-slot half page (512 B apart), z = 64-dim block (128 B
 // apart), w = half page of one KV head ((page * 4 + head) * 2 + half, 4 KB
 // apart), with the 128-byte swizzle.  A box of {64, 8, 4, 2} is one page of
 // one head (8 contiguous KB), landing as [half][block][8 slots][128 B]: two
-// 8-row groups of the group-major K tile or of a V page slot.
-bool ring_map(CUtensorMap* map, const void* cache, int pool_pages) {
+// 8-row groups of the group-major K tile or of a V page slot (both bf16 kernels).
+bool bf16_page_map(CUtensorMap* map, const void* cache, int pool_pages) {
   auto fn = ring_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {64, 8, 4, (cuuint64_t)pool_pages * kHkv * 2};
@@ -37,8 +39,6 @@ bool ring_map(CUtensorMap* map, const void* cache, int pool_pages) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 TcPlan ring_plan(int max_nodes) {
   TcPlan pl;
@@ -55,7 +55,7 @@ TcPlan ring_plan(int max_nodes) {
 
 cudaError_t launch_attn_ring(const AttnParams& p, const BatchDesc& bd, cudaStream_t st) {
   CUtensorMap mk, mv;
-  if (!ring_map(&mk, p.k_cache, p.num_pool_pages) || !ring_map(&mv, p.v_cache, p.num_pool_pages))
+  if (!bf16_page_map(&mk, p.k_cache, p.num_pool_pages) || !bf16_page_map(&mv, p.v_cache, p.num_pool_pages))
     return cudaErrorInvalidValue;
   const TcPlan pl = ring_plan(bd.max_nodes);
   const cudaError_t e = p.window > 0 ? launch_ring_window(mk, mv, p, bd, pl, st)

@@ -15,6 +15,8 @@ struct TcPlan {
 };
 // bf16 caches: the ring-buffered kernel (attn_ring_kernel.cuh), up to 144 query columns per CTA.
 constexpr int kRingMaxNQ = 144;
+// The bf16 page tensor map both bf16 kernels load through (one 8 KB page of one KV head per box).
+bool bf16_page_map(CUtensorMap* map, const void* cache, int pool_pages);
 TcPlan ring_plan(int max_nodes);
 cudaError_t launch_attn_ring(const AttnParams& p, const BatchDesc& bd, cudaStream_t st);
 // its sliding-window instances (attn_ring_win.cu)

@@ -110,15 +110,6 @@ __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* m
       : "memory");
 }
 
-// One 64-dim block of one page of one KV head (16 slots x 128 B = 2 KB): the
-// 4-D box {64, 8, 1, 2} of the cache map at block z, outer coordinate w.
-__device__ __forceinline__ void tma_load_kblk(uint32_t dst, const CUtensorMap* map, int z, int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
 // ------------------------------------------------------------ tcgen05
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
