@@ -405,7 +405,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
               ok = false;
               break;
             }
-            __nanosleep(20);
+            // no sleep between polls: the loader's wake-up would sit on the widening chain
           }
         }
         // early context loads: the next slots free up only as the compute warps (which wait) progress
@@ -731,7 +731,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             report(p.dev_status, SD_DEV_TIMEOUT);
             break;
           }
-          __nanosleep(32);
+          // e4m3 caches: no sleep between polls (the issue sits on the per-tile chain; 32K tree layer
+          // 69.4 -> 67.7 us); bf16 caches keep a short one (measured marginally faster there)
+          if constexpr (!KV8) __nanosleep(32);
         }
       }
     }
